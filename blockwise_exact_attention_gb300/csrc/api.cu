@@ -1,0 +1,347 @@
+// C ABI of libbea: argument validation, tensor-map construction and kernel
+// dispatch. Every check runs before any CUDA call, so a rejected request
+// touches neither the device nor the stream.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/bea.h"
+#include "common.cuh"
+#include "status.cuh"
+
+namespace {
+
+using bea::AttnDims;
+using bea::Lse3;
+using bea::Seq4;
+
+thread_local int g_last_launches = 0;
+
+// Status word of each device the library runs on: kernels OR flags into it.
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int status_ptr_for_current_device(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BEA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || p == nullptr) return BEA_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return BEA_OK;
+}
+
+int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        fn == nullptr || q != cudaDriverEntryPointSuccess)
+      return BEA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return BEA_OK;
+}
+
+int64_t esize(int32_t dtype) { return dtype == BEA_BF16 ? 2 : 4; }
+
+bool valid_dtype(int32_t dt) { return dt == BEA_BF16 || dt == BEA_F32; }
+
+int64_t numel(const bea_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+// Structural checks of one tensor: rank, dtype, non-negative shape/strides,
+// contiguous last dim, 16-byte aligned base and strides (when non-empty).
+int check_tensor(const bea_tensor* t, int ndim) {
+  if (t == nullptr) return BEA_ERR_ARG;
+  if (t->ndim != ndim) return BEA_ERR_SHAPE;
+  if (!valid_dtype(t->dtype)) return BEA_ERR_DTYPE;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0 || t->shape[i] > (int64_t(1) << 31) - 1) return BEA_ERR_SHAPE;
+    if (t->stride[i] < 0) return BEA_ERR_ALIGN;
+  }
+  if (numel(t) == 0) return BEA_OK;
+  if (t->data == nullptr) return BEA_ERR_ARG;
+  const int64_t es = esize(t->dtype);
+  if (t->shape[ndim - 1] > 1 && t->stride[ndim - 1] != 1) return BEA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return BEA_ERR_ALIGN;
+  for (int i = 0; i < ndim - 1; ++i)
+    if (t->shape[i] > 1 && (t->stride[i] * es) % 16 != 0) return BEA_ERR_ALIGN;
+  return BEA_OK;
+}
+
+bool same_shape(const bea_tensor* a, const bea_tensor* b) {
+  if (a->ndim != b->ndim) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i]) return false;
+  return true;
+}
+
+Seq4 seq4(const bea_tensor* t) { return Seq4{t->data, t->stride[0], t->stride[1], t->stride[2]}; }
+Lse3 lse3(const bea_tensor* t) { return Lse3{static_cast<float*>(t->data), t->stride[0], t->stride[1]}; }
+
+int check_window(int is_causal, int wl, int wr, int* ewl, int* ewr) {
+  if (wl < -1 || wr < -1) return BEA_ERR_ARG;
+  if (is_causal != 0 && is_causal != 1) return BEA_ERR_ARG;
+  if (is_causal && wr > 0) return BEA_ERR_ARG;
+  *ewl = wl;
+  *ewr = is_causal ? 0 : wr;
+  return BEA_OK;
+}
+
+// Shared validation of q, k, v (and the mask) for forward and backward.
+int check_qkv(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, float scale, int is_causal, int wl,
+              int wr, AttnDims* a) {
+  int rc;
+  if ((rc = check_tensor(q, 4)) || (rc = check_tensor(k, 4)) || (rc = check_tensor(v, 4))) return rc;
+  if (q->dtype != k->dtype || q->dtype != v->dtype) return BEA_ERR_DTYPE;
+  if (!same_shape(k, v)) return BEA_ERR_SHAPE;
+  if (k->shape[0] != q->shape[0] || k->shape[3] != q->shape[3]) return BEA_ERR_SHAPE;
+  const int64_t h = q->shape[2], hkv = k->shape[2];
+  if (hkv <= 0 || h % hkv != 0) return BEA_ERR_SHAPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return BEA_ERR_ARG;
+  int ewl, ewr;
+  if ((rc = check_window(is_causal, wl, wr, &ewl, &ewr))) return rc;
+  if ((ewl >= 0 || ewr >= 0) && q->shape[1] != k->shape[1]) return BEA_ERR_SHAPE;
+  const int64_t d = q->shape[3];
+  if (q->dtype == BEA_BF16) {
+    if (d != 64 && d != 128) return BEA_ERR_UNSUPPORTED;
+  } else {
+    if (d < 4 || d > 128 || d % 4 != 0) return BEA_ERR_UNSUPPORTED;
+  }
+  if (q->shape[0] * h > (int64_t(1) << 31) - 1) return BEA_ERR_SHAPE;
+  a->n = (int)q->shape[0];
+  a->lq = (int)q->shape[1];
+  a->lk = (int)k->shape[1];
+  a->h = (int)h;
+  a->hkv = (int)hkv;
+  a->d = (int)d;
+  a->wl = ewl;
+  a->wr = ewr;
+  a->scale = scale;
+  return BEA_OK;
+}
+
+int check_lse(const bea_tensor* lse, const AttnDims& a) {
+  int rc;
+  if ((rc = check_tensor(lse, 3))) return rc;
+  if (lse->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  if (lse->shape[0] != a.n || lse->shape[1] != a.h || lse->shape[2] != a.lq) return BEA_ERR_SHAPE;
+  return BEA_OK;
+}
+
+// [n, l, h, d] bf16 tensor -> TMA descriptor with 64-column (128-byte) boxes
+// of 128 rows, 128-byte swizzled (the layout the MMA descriptors expect).
+int make_seq_map(const bea_tensor* t, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = get_encoder(&enc);
+  if (rc) return rc;
+  const int64_t d = t->shape[3], hh = t->shape[2], l = t->shape[1], n = t->shape[0];
+  const int64_t es = 2;
+  // A size-1 dimension never moves the address; give it a harmless stride.
+  const cuuint64_t s_h = (hh > 1) ? t->stride[2] * es : d * es;
+  const cuuint64_t s_l = (l > 1) ? t->stride[1] * es : s_h * hh;
+  const cuuint64_t s_n = (n > 1) ? t->stride[0] * es : s_l * l;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)hh, (cuuint64_t)l, (cuuint64_t)n};
+  cuuint64_t strides[3] = {s_h, s_l, s_n};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t es1[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es1,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BEA_OK : BEA_ERR_CUDA;
+}
+
+int finish(cudaError_t e, int launches) {
+  if (e != cudaSuccess) return BEA_ERR_CUDA;
+  g_last_launches = launches;
+  return BEA_OK;
+}
+
+// Workspace layout of the backward: [dq_acc | D | lse2], each 256-byte aligned.
+struct BwdWorkspace {
+  size_t dq_off, d_off, l_off, total;
+};
+BwdWorkspace bwd_workspace_layout(int64_t n, int64_t lq, int64_t h, int64_t d) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const int64_t lq_pad = (lq + 127) / 128 * 128;
+  BwdWorkspace w;
+  w.dq_off = 0;
+  w.d_off = up((size_t)(n * h * lq_pad * d) * 4);
+  w.l_off = w.d_off + up((size_t)(n * h * lq_pad) * 4);
+  w.total = w.l_off + up((size_t)(n * h * lq_pad) * 4);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bea_version(void) { return BEA_VERSION; }
+
+int bea_last_launch_count(void) { return g_last_launches; }
+
+const char* bea_status_string(int code) {
+  switch (code) {
+    case BEA_OK: return "ok";
+    case BEA_ERR_ARG: return "invalid argument (null pointer, scale, window or flag)";
+    case BEA_ERR_SHAPE: return "inconsistent tensor shapes";
+    case BEA_ERR_DTYPE: return "dtype not allowed for this argument";
+    case BEA_ERR_ALIGN: return "pointer or stride not 16-byte aligned, or last dimension not contiguous";
+    case BEA_ERR_UNSUPPORTED: return "unsupported configuration (head dim or dtype combination)";
+    case BEA_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case BEA_ERR_TIMEOUT: return "a kernel wait ran past its time limit";
+    case BEA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out,
+                      const bea_tensor* lse, float softmax_scale, int is_causal, int window_left, int window_right,
+                      void* stream) {
+  AttnDims a;
+  int rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_tensor(out, 4))) return rc;
+  if (!same_shape(out, q)) return BEA_ERR_SHAPE;
+  if ((rc = check_lse(lse, a))) return rc;
+  if (q->dtype == BEA_F32 && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  if (a.n == 0 || a.h == 0 || a.lq == 0) return finish(cudaSuccess, 0);
+  if (q->dtype == BEA_F32) {
+    bea::F32FwdParams p{a, seq4(q), seq4(k), seq4(v), seq4(out), lse3(lse)};
+    return finish(bea::launch_fwd_f32(p, s, &launches), launches);
+  }
+  bea::FwdParams p;
+  p.a = a;
+  p.out = seq4(out);
+  p.out_is_f32 = out->dtype == BEA_F32;
+  p.lse = lse3(lse);
+  if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  CUtensorMap tq, tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if ((rc = make_seq_map(q, &tq))) return rc;
+  if (a.lk > 0) {
+    if ((rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv))) return rc;
+  }
+  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, s, &launches), launches);
+}
+
+size_t bea_flash_mha_bwd_workspace_size(int64_t n, int64_t lq, int64_t h, int64_t d) {
+  if (n < 0 || lq < 0 || h < 0 || d < 0) return 0;
+  return bwd_workspace_layout(n, lq, h, d).total;
+}
+
+int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k, const bea_tensor* v,
+                      const bea_tensor* out, const bea_tensor* lse, const bea_tensor* dq, const bea_tensor* dk,
+                      const bea_tensor* dv, float softmax_scale, int is_causal, int window_left, int window_right,
+                      int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  AttnDims a;
+  int rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(out, 4)) || (rc = check_tensor(dq, 4)) ||
+      (rc = check_tensor(dk, 4)) || (rc = check_tensor(dv, 4)))
+    return rc;
+  if (!same_shape(dout, q) || !same_shape(out, q) || !same_shape(dq, q) || !same_shape(dk, k) ||
+      !same_shape(dv, k))
+    return BEA_ERR_SHAPE;
+  if ((rc = check_lse(lse, a))) return rc;
+  if (accumulate != 0 && accumulate != 1) return BEA_ERR_ARG;
+  if (dout->dtype != q->dtype) return BEA_ERR_DTYPE;
+  if (out->dtype != q->dtype && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  const bool f32 = q->dtype == BEA_F32;
+  for (const bea_tensor* g : {dq, dk, dv}) {
+    if (accumulate && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
+    if (f32 && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  }
+  if (f32 && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  const BwdWorkspace w = bwd_workspace_layout(a.n, a.lq, a.h, a.d);
+  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < w.total)
+    return BEA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  if (a.n == 0 || a.h == 0) return finish(cudaSuccess, 0);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (f32) {
+    bea::F32BwdParams p{a,        seq4(dout), seq4(q),   seq4(k),
+                        seq4(v),  seq4(out),  seq4(dq),  seq4(dk),
+                        seq4(dv), lse3(lse),  reinterpret_cast<float*>(ws + w.d_off), accumulate};
+    return finish(bea::launch_bwd_f32(p, s, &launches), launches);
+  }
+  return BEA_ERR_UNSUPPORTED;
+}
+
+int bea_ring_merge(const bea_tensor* out_acc, const bea_tensor* lse_acc, const bea_tensor* out_blk,
+                   const bea_tensor* lse_blk, const bea_tensor* out_final, void* stream) {
+  int rc;
+  if ((rc = check_tensor(out_acc, 4)) || (rc = check_tensor(lse_acc, 3)) || (rc = check_tensor(out_blk, 4)) ||
+      (rc = check_tensor(lse_blk, 3)))
+    return rc;
+  if (out_acc->dtype != BEA_F32 || lse_acc->dtype != BEA_F32 || lse_blk->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  if (!same_shape(out_acc, out_blk) || !same_shape(lse_acc, lse_blk)) return BEA_ERR_SHAPE;
+  const int64_t n = out_acc->shape[0], l = out_acc->shape[1], h = out_acc->shape[2], d = out_acc->shape[3];
+  if (lse_acc->shape[0] != n || lse_acc->shape[1] != h || lse_acc->shape[2] != l) return BEA_ERR_SHAPE;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return BEA_ERR_UNSUPPORTED;
+  if (out_final != nullptr) {
+    if ((rc = check_tensor(out_final, 4))) return rc;
+    if (out_final->dtype != BEA_BF16) return BEA_ERR_DTYPE;
+    if (!same_shape(out_final, out_acc)) return BEA_ERR_SHAPE;
+  }
+  bea::MergeParams p;
+  p.n = (int)n;
+  p.l = (int)l;
+  p.h = (int)h;
+  p.d = (int)d;
+  p.acc = seq4(out_acc);
+  p.lse_acc = lse3(lse_acc);
+  p.blk = seq4(out_blk);
+  p.blk_is_f32 = out_blk->dtype == BEA_F32;
+  p.lse_blk = lse3(lse_blk);
+  p.fin = out_final ? seq4(out_final) : Seq4{nullptr, 0, 0, 0};
+  int launches = 0;
+  return finish(bea::launch_ring_merge(p, static_cast<cudaStream_t>(stream), &launches), launches);
+}
+
+int bea_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return BEA_ERR_CUDA;
+  uint32_t* dptr = nullptr;
+  if (status_ptr_for_current_device(&dptr)) return BEA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, dptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return BEA_ERR_CUDA;
+  if (cudaMemset(dptr, 0, sizeof(word)) != cudaSuccess) return BEA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return BEA_ERR_CUDA;
+  if (word & bea::BEA_STATUS_TIMEOUT) return BEA_ERR_TIMEOUT;
+  if (word & bea::BEA_STATUS_CONFIG) return BEA_ERR_UNSUPPORTED;
+  return BEA_OK;
+}
+
+int bea_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 2000000) return BEA_ERR_ARG;
+  uint32_t* dptr = nullptr;
+  if (status_ptr_for_current_device(&dptr)) return BEA_ERR_CUDA;
+  return finish(bea::launch_selftest_wait_timeout(dptr, (uint64_t)limit_us * 1000ull,
+                                                  static_cast<cudaStream_t>(stream)),
+                1);
+}
+
+}  // extern "C"

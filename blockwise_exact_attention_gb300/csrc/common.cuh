@@ -1,0 +1,77 @@
+// Parameter blocks shared by the host dispatch (api.cu) and the kernels, and
+// the kernel launchers each translation unit exports.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bea {
+
+// A [n, l, h, d] tensor with a contiguous last dimension (strides in elements).
+struct Seq4 {
+  void* ptr;
+  int64_t sn, sl, sh;
+};
+
+// A [n, h, l] fp32 tensor with a contiguous last dimension.
+struct Lse3 {
+  float* ptr;
+  int64_t sn, sh;
+};
+
+struct AttnDims {
+  int n, lq, lk, h, hkv, d;
+  int wl, wr;  // effective window: -1 unbounded; causal already folded into wr = 0
+  float scale;
+};
+
+// Key j is visible to query i (inclusive window reading; causal = right 0).
+__host__ __device__ __forceinline__ bool key_visible(int i, int j, int wl, int wr) {
+  return (wl < 0 || j >= i - wl) && (wr < 0 || j <= i + wr);
+}
+
+// ---- ring merge --------------------------------------------------------------
+struct MergeParams {
+  int n, l, h, d;
+  Seq4 acc;  // f32
+  Lse3 lse_acc;
+  Seq4 blk;  // bf16 or f32
+  int blk_is_f32;
+  Lse3 lse_blk;
+  Seq4 fin;  // bf16, ptr may be null
+};
+cudaError_t launch_ring_merge(const MergeParams& p, cudaStream_t s, int* nlaunch);
+
+// ---- fp32 SIMT path ------------------------------------------------------------
+struct F32FwdParams {
+  AttnDims a;
+  Seq4 q, k, v, out;  // all f32
+  Lse3 lse;
+};
+cudaError_t launch_fwd_f32(const F32FwdParams& p, cudaStream_t s, int* nlaunch);
+
+struct F32BwdParams {
+  AttnDims a;
+  Seq4 dout, q, k, v, out, dq, dk, dv;  // all f32
+  Lse3 lse;
+  float* D;  // workspace [n, h, lq]
+  int accumulate;
+};
+cudaError_t launch_bwd_f32(const F32BwdParams& p, cudaStream_t s, int* nlaunch);
+
+// ---- bf16 tensor-core path -------------------------------------------------------
+struct FwdParams {
+  AttnDims a;
+  Seq4 out;
+  int out_is_f32;
+  Lse3 lse;
+  uint32_t* status;
+};
+// Tensor maps are built by the caller (api.cu) over q, k, v.
+cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, cudaStream_t s, int* nlaunch);
+
+cudaError_t launch_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace bea

@@ -1,0 +1,472 @@
+// Blockwise exact attention forward on sm_103a tensor cores (bf16 in, fp32
+// accumulation), emitting O and the per-row log-sum-exp L.
+//
+// What it computes is picotron context_parallel.py, ring_attention_forward
+// (S = scale Q K^T, causal/window mask, softmax, L, P V), reorganised as the
+// blockwise online softmax: K/V are visited one 128-key tile at a time and
+// each query row keeps a running max m and running sum l, so S never leaves
+// the SM. The result is the same up to rounding order; P is rounded to bf16
+// before the P V product.
+//
+// One CTA owns 256 query rows (two 128-row subtiles) of one (batch, head):
+//   warp 8      TMA producer: Q once, then K_j / V_j into an NS-stage ring;
+//   warp 9      MMA issuer (one lane): S_t = Q_t K_j^T into TMEM (both
+//               operands in shared memory), O_t += P_t V_j with P_t read
+//               from TMEM;
+//   warps 0-3   softmax for subtile 0, warps 4-7 for subtile 1: one thread
+//               per query row (TMEM lane), online softmax, P written back to
+//               TMEM over S as packed bf16, O rescaled in TMEM only when the
+//               row max grows by more than 2^8, and the final epilogue.
+// The MMA issue order S_0(j), S_1(j), PV_0(j), S_0(j+1), PV_1(j), S_1(j+1),
+// ... lets each softmax group work while the tensor core serves the other
+// subtile. Tiles outside the causal/window band are never loaded or computed;
+// only tiles that straddle the band edge (or the ragged end of K) are masked
+// element by element.
+//
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [384,384+D); P_t occupies the first 64 columns of S_t. S_t(j+1)
+// overwrites P_t(j) only after PV_t(j), which the single issuing thread
+// placed before it in the MMA pipeline.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace bea {
+namespace {
+
+constexpr int kBlockM = 128;  // rows per subtile (= TMEM lanes)
+constexpr int kBlockN = 128;  // keys per tile
+constexpr int kSub = 2;       // subtiles per CTA
+constexpr int kThreads = 384;  // 3 warpgroups
+// Register split: launched at kRegsLaunch per thread (65536 / 384 rounded
+// down to 8); the softmax warpgroups raise to kRegsSoftmax and the
+// producer/MMA warpgroup lowers to kRegsOther, which sums to the launch:
+// 256 * 216 + 128 * 72 = 384 * 168.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsOther = 72;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch, "register split");
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kBoxes = D / 64;          // 64-column (128-byte) TMA boxes per row
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kSub * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kNumBars = 1 + 3 * kStages + 3 * kSub + 1;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+  static constexpr uint32_t kVLbo = 64 * 128 * 2;  // byte distance of 64-column V blocks
+};
+
+struct Sched {
+  int lo[kSub], hi[kSub];  // K tile range per subtile (empty if lo >= hi)
+  int lo_all, hi_all;
+  int q0;
+};
+
+__device__ __forceinline__ void tile_range(const AttnDims& a, int qs, int& lo, int& hi) {
+  lo = hi = 0;
+  if (qs >= a.lq) return;
+  const int qe = min(qs + kBlockM, a.lq);
+  const int kmin = (a.wl < 0) ? 0 : max(0, qs - a.wl);
+  const int kmax = (a.wr < 0) ? a.lk : min(a.lk, qe - 1 + a.wr + 1);
+  if (kmax <= kmin) return;
+  lo = kmin / kBlockN;
+  hi = (kmax + kBlockN - 1) / kBlockN;
+}
+
+// Does tile j need per-element masking for subtile rows [qs, qs+128)?
+__device__ __forceinline__ bool tile_needs_mask(const AttnDims& a, int qs, int j) {
+  const int k0 = j * kBlockN, k1 = k0 + kBlockN - 1;
+  if (k1 >= a.lk) return true;
+  const int q1 = qs + kBlockM - 1;
+  if (a.wl >= 0 && k0 < q1 - a.wl) return true;
+  if (a.wr >= 0 && k1 > qs + a.wr) return true;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const FwdParams p, float scale_log2) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + C::kStages;
+  uint64_t* kv_empty = v_full + C::kStages;
+  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* p_full = s_full + kSub;
+  uint64_t* o_full = p_full + kSub;
+  uint64_t* mma_done = o_full + kSub;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const AttnDims& a = p.a;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work decomposition: longest (latest) query blocks first ----
+  const int nqb = (a.lq + kSub * kBlockM - 1) / (kSub * kBlockM);
+  const int bh_count = a.n * a.h;
+  const int qb = nqb - 1 - (int)(blockIdx.x / bh_count);
+  const int bh = blockIdx.x % bh_count;
+  const int b = bh / a.h, hq = bh % a.h, kvh = hq / (a.h / a.hkv);
+  Sched sc;
+  sc.q0 = qb * kSub * kBlockM;
+  sc.lo_all = 1 << 30;
+  sc.hi_all = -1;
+#pragma unroll
+  for (int t = 0; t < kSub; ++t) {
+    tile_range(a, sc.q0 + t * kBlockM, sc.lo[t], sc.hi[t]);
+    if (sc.lo[t] < sc.hi[t]) {
+      sc.lo_all = min(sc.lo_all, sc.lo[t]);
+      sc.hi_all = max(sc.hi_all, sc.hi[t]);
+    }
+  }
+  if (sc.hi_all < 0) sc.lo_all = sc.hi_all = 0;
+
+  // ---- setup ----
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < kSub; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kBlockM);
+      mbar_init(&o_full[t], 1);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  if (warp == kProducerWarp) {
+    // ========================== TMA producer ==========================
+    if (lane == 0) {
+      if (sc.hi_all > sc.lo_all) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+      }
+      uint32_t qbytes = 0;
+      for (int t = 0; t < kSub; ++t)
+        if (sc.lo[t] < sc.hi[t]) qbytes += C::kTileBytes;
+      if (qbytes) {
+        mbar_arrive_expect_tx(q_full, qbytes);
+        for (int t = 0; t < kSub; ++t) {
+          if (sc.lo[t] >= sc.hi[t]) continue;
+          uint8_t* dst = smem + C::kQOff + t * C::kTileBytes;
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(dst + x * 16384, &tq, q_full, x * 64, hq, sc.q0 + t * kBlockM, b);
+        }
+      }
+      const uint64_t pol = l2_policy_evict_last();
+      int it = 0;
+      for (int j = sc.lo_all; j < sc.hi_all; ++j, ++it) {
+        const int s = it % C::kStages;
+        if (it >= C::kStages) {
+          if (!wait_parity(&kv_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, p.status)) break;
+        }
+        uint8_t* kd = smem + C::kKOff + s * C::kTileBytes;
+        uint8_t* vd = smem + C::kVOff + s * C::kTileBytes;
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d_hint(kd + x * 16384, &tk, &k_full[s], x * 64, kvh, j * kBlockN, b, pol);
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d_hint(vd + x * 16384, &tv, &v_full[s], x * 64, kvh, j * kBlockN, b, pol);
+      }
+      // Loads still in flight must land before the CTA's shared memory goes away.
+      const int issued = it;
+      for (int k = max(0, issued - C::kStages); k < issued; ++k) {
+        const int s = k % C::kStages;
+        const uint32_t par = (k / C::kStages) & 1;
+        volatile int no_abort = 0;
+        wait_parity(&k_full[s], par, &no_abort, p.status, 200000000ull);
+        wait_parity(&v_full[s], par, &no_abort, p.status, 200000000ull);
+      }
+      if (qbytes) {
+        volatile int no_abort = 0;
+        wait_parity(q_full, 0, &no_abort, p.status, 200000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ========================== MMA issuer ==========================
+    if (lane == 0) {
+      const uint32_t q_addr = smem_u32(smem + C::kQOff);
+      const uint32_t k_addr = smem_u32(smem + C::kKOff);
+      const uint32_t v_addr = smem_u32(smem + C::kVOff);
+      int pv_count[kSub] = {0, 0};
+      bool ok = true;
+      auto issue_s = [&](int t, int s) {
+        const uint32_t qa = q_addr + t * C::kTileBytes;
+        const uint32_t ka = k_addr + s * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          umma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), C::kIdescS,
+                  k > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int s) {
+        const uint32_t va = v_addr + s * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kBlockN / 16; ++k) {
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_sw128(va + k * 2048, C::kVLbo, 1024),
+                  C::kIdescPV, (pv_count[t] > 0 || k > 0) ? 1u : 0u);
+        }
+        ++pv_count[t];
+      };
+      auto active = [&](int t, int j) { return j >= sc.lo[t] && j < sc.hi[t]; };
+
+      if (sc.hi_all > sc.lo_all) {
+        ok = wait_parity(q_full, 0, abort_flag, p.status);
+        if (ok) ok = wait_parity(&k_full[0], 0, abort_flag, p.status);
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < kSub; ++t)
+            if (active(t, sc.lo_all)) issue_s(t, 0);
+        }
+        int it = 0;
+        for (int j = sc.lo_all; ok && j < sc.hi_all; ++j, ++it) {
+          const int s = it % C::kStages;
+          const uint32_t par = (it / C::kStages) & 1;
+          const int s1 = (it + 1) % C::kStages;
+          const uint32_t par1 = ((it + 1) / C::kStages) & 1;
+          bool k_next_ready = false;
+          if (!(ok = wait_parity(&v_full[s], par, abort_flag, p.status))) break;
+          for (int t = 0; t < kSub && ok; ++t) {
+            if (!active(t, j)) continue;
+            if (!(ok = wait_parity(&p_full[t], pv_count[t] & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_pv(t, s);
+            if (j + 1 < sc.hi_all && active(t, j + 1)) {
+              if (!k_next_ready) {
+                if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              issue_s(t, s1);
+            }
+          }
+          if (!ok) break;
+          // a subtile whose band starts at tile j+1 still needs its first S
+          for (int t = 0; t < kSub && ok; ++t) {
+            if (j + 1 < sc.hi_all && !active(t, j) && active(t, j + 1)) {
+              if (!k_next_ready) {
+                if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              issue_s(t, s1);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&kv_empty[s]);
+          for (int t = 0; t < kSub; ++t)
+            if (j == sc.hi[t] - 1) umma_commit(&o_full[t]);
+        }
+      }
+      // Everything issued must finish before TMEM is released.
+      umma_commit(mma_done);
+      volatile int no_abort = 0;
+      wait_parity(mma_done, 0, &no_abort, p.status, 200000000ull);
+    }
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    // ========================== softmax groups ==========================
+    const int t = warp / 4;           // subtile
+    const int r = threadIdx.x % 128;  // row within subtile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_base + t * 128;
+    const uint32_t o_tmem = tmem + lane_base + 256 + t * 128;
+    const int qs = sc.q0 + t * kBlockM;
+    const int qi = qs + r;
+    float m_ref = -INFINITY;  // running max, log2 domain
+    float l_sum = 0.f;
+    bool ok = true;
+    int it = 0;
+    for (int j = sc.lo[t]; j < sc.hi[t]; ++j, ++it) {
+      if (!(ok = wait_parity(&s_full[t], it & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld32(s_tmem + 0, sr);
+      tmem_ld32(s_tmem + 32, sr + 32);
+      tmem_ld32(s_tmem + 64, sr + 64);
+      tmem_ld32(s_tmem + 96, sr + 96);
+      tmem_wait_ld();
+      reg_fence<128>(sr);
+      if (tile_needs_mask(a, qs, j)) {
+        const int k0 = j * kBlockN;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int kj = k0 + c;
+          if (!(kj < a.lk && key_visible(qi, kj, a.wl, a.wr))) sr[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      // softmax_scale > 0, so the max commutes with the scaling
+      float mx = __uint_as_float(sr[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      mx *= scale_log2;
+      const float m_new = fmaxf(m_ref, mx);
+      const bool grow = m_new > m_ref + kRescaleThreshold;  // also true when m_ref = -inf, m_new finite
+      float f = 1.f;
+      bool rescale = false;
+      if (it == 0) {
+        m_ref = m_new;  // the first P V overwrites O, nothing to rescale
+      } else {
+        rescale = __any_sync(0xffffffffu, grow);
+        if (grow) {
+          f = ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          l_sum *= f;
+        }
+      }
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      uint32_t pk[64];
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, neg_m));
+        psum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l_sum += psum;
+      tmem_st32(s_tmem + 0, pk);
+      tmem_st32(s_tmem + 32, pk + 32);
+      if (rescale) {
+        // PV_t(j-1) has completed: s_full for tile j was committed after it.
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t orow[32];
+          tmem_ld32(o_tmem + c0, orow);
+          tmem_wait_ld();
+          reg_fence<32>(orow);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * f);
+          tmem_st32(o_tmem + c0, orow);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    // ---- epilogue ----
+    const bool have_o = sc.lo[t] < sc.hi[t];
+    if (ok && have_o) ok = wait_parity(&o_full[t], 0, abort_flag, p.status);
+    if (ok && qs < a.lq) {
+      tc_fence_after();
+      const bool row_ok = qi < a.lq;
+      const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t orow[32];
+        if (have_o) {
+          tmem_ld32(o_tmem + c0, orow);
+          tmem_wait_ld();
+          reg_fence<32>(orow);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orow[c] = 0u;
+        }
+        if (row_ok) {
+          if (p.out_is_f32) {
+            float* dst = reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn + (int64_t)qi * p.out.sl +
+                         hq * p.out.sh + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 v4 = make_float4(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv,
+                                            __uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
+              *reinterpret_cast<float4*>(dst + c) = v4;
+            }
+          } else {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out.ptr) + b * p.out.sn +
+                                 (int64_t)qi * p.out.sl + hq * p.out.sh + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v4;
+              v4.x = pack_bf16x2(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv);
+              v4.y = pack_bf16x2(__uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
+              v4.z = pack_bf16x2(__uint_as_float(orow[c + 4]) * inv, __uint_as_float(orow[c + 5]) * inv);
+              v4.w = pack_bf16x2(__uint_as_float(orow[c + 6]) * inv, __uint_as_float(orow[c + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c) = v4;
+            }
+          }
+        }
+      }
+      if (row_ok) {
+        const float L = (l_sum > 0.f) ? (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f : -INFINITY;
+        p.lse.ptr[b * p.lse.sn + hq * p.lse.sh + qi] = L;
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         cudaStream_t s, int* nlaunch) {
+  using C = FwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // The register split above is only sound at exactly kRegsLaunch registers
+  // per thread; refuse to launch otherwise (setmaxnreg.inc would never return).
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  const int nqb = (p.a.lq + kSub * kBlockM - 1) / (kSub * kBlockM);
+  const long long blocks = (long long)nqb * p.a.n * p.a.h;
+  if (blocks == 0) return cudaSuccess;
+  const float scale_log2 = p.a.scale * 1.4426950408889634f;
+  fwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, p, scale_log2);
+  *nlaunch += 1;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            cudaStream_t s, int* nlaunch) {
+  if (p.a.d == 128) return launch_fwd_d<128>(p, tq, tk, tv, s, nlaunch);
+  if (p.a.d == 64) return launch_fwd_d<64>(p, tq, tk, tv, s, nlaunch);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bea

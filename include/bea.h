@@ -1,0 +1,188 @@
+/*
+ * bea.h — C ABI of the blockwise exact attention library (libbea.so).
+ *
+ * Exact softmax attention computed block by block with an online softmax on
+ * one GB300 (sm_103a), its backward pass recomputed from the per-row
+ * log-sum-exp, and the log-sum-exp merge that folds a partial (out, lse) from
+ * one K/V block into a running (out, lse) — the step ring attention repeats
+ * once per K/V rotation.
+ *
+ * Tensors.
+ *   Every tensor is described by a bea_tensor: a DEVICE pointer, a dtype, a
+ *   rank, a shape and strides in ELEMENTS. The caller owns every buffer; the
+ *   library never allocates, frees or keeps a pointer after a call returns.
+ *   Sequence tensors are [n, l, h, d] (batch, sequence, heads, head dim) with
+ *   the last dimension contiguous (stride 1), the base pointer 16-byte
+ *   aligned and the other strides multiples of 16 bytes, so that chunk views
+ *   of a longer sequence (an offset base pointer with the parent's strides)
+ *   are accepted without a copy. The log-sum-exp is [n, h, l] fp32, natural
+ *   log, softmax_scale included, with a contiguous last dimension
+ *   (flash_attn_jax flash_sharding.py, sections "Sharding" and "Ring
+ *   Forward": out [n,l,h,d], lse [n,h,l]).
+ *
+ * Grouped-query attention.
+ *   q has h heads, k and v have h_kv heads with h % h_kv == 0; query head i
+ *   reads K/V head i / (h / h_kv) (picotron context_parallel.py,
+ *   RingAttention._repeat_kv), without expanding K/V in memory.
+ *
+ * Masks.
+ *   is_causal: query i sees key j only if j <= i (picotron
+ *   ring_attention_forward: the upper triangle is masked).
+ *   window (left, right), -1 meaning unbounded: key j is visible to query i
+ *   iff (left < 0 || j >= i - left) && (right < 0 || j <= i + right). The
+ *   pages only ever pass (-1, -1); this inclusive reading is the library's.
+ *   is_causal forces right = 0; right > 0 together with is_causal is an
+ *   argument error. Causal or windowed calls need lq == lk.
+ *   A query row that sees no key gets out = 0 and lse = -inf.
+ *
+ * Streams and errors.
+ *   `stream` is a cudaStream_t (NULL = legacy default stream) of the current
+ *   device. Every call validates all arguments on the host first and
+ *   launches nothing when a check fails. Launches are asynchronous. Return
+ *   values: BEA_OK or one of the negative BEA_ERR_* codes. No kernel traps:
+ *   a kernel whose internal wait runs past its time limit ORs a flag into a
+ *   per-device status word, which bea_get_device_status() reads.
+ *
+ * Thread safety: calls may come from several host threads; the library's
+ * only host state is a per-device cache filled on first use.
+ */
+#ifndef BEA_H_
+#define BEA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BEA_VERSION 1
+
+typedef enum bea_dtype {
+  BEA_BF16 = 0, /* bfloat16 */
+  BEA_F32 = 1   /* float32 */
+} bea_dtype;
+
+typedef enum bea_status {
+  BEA_OK = 0,
+  BEA_ERR_ARG = -1,         /* null pointer, bad scalar (scale, window, flags) */
+  BEA_ERR_SHAPE = -2,       /* shapes inconsistent with each other */
+  BEA_ERR_DTYPE = -3,       /* dtype not allowed for this argument */
+  BEA_ERR_ALIGN = -4,       /* pointer or stride not 16-byte aligned, last dim not contiguous */
+  BEA_ERR_UNSUPPORTED = -5, /* valid request this build does not implement (e.g. head dim) */
+  BEA_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed */
+  BEA_ERR_TIMEOUT = -7,     /* a kernel wait ran past its limit (from bea_get_device_status) */
+  BEA_ERR_WORKSPACE = -8    /* workspace missing, misaligned or too small */
+} bea_status;
+
+typedef struct bea_tensor {
+  void* data;        /* device pointer to element [0,0,0,0] */
+  int32_t dtype;     /* bea_dtype */
+  int32_t ndim;      /* 4 for [n,l,h,d] tensors, 3 for [n,h,l] lse tensors */
+  int64_t shape[4];  /* first ndim entries used */
+  int64_t stride[4]; /* in elements; first ndim entries used */
+} bea_tensor;
+
+/*
+ * Forward: out = softmax(softmax_scale * q k^T + mask) v and
+ * lse = log(sum_j exp(softmax_scale * q.k_j + mask_j)) per query row
+ * (picotron context_parallel.py, ring_attention_forward; flash_attn_jax
+ * flash_sharding.py, the local fwd(q, k, v) of partition_fwd).
+ *
+ *   q    [n, lq, h, d]     bf16 or f32
+ *   k, v [n, lk, h_kv, d]  same dtype as q
+ *   out  [n, lq, h, d]     bf16 q: bf16 or f32; f32 q: f32 (written)
+ *   lse  [n, h, lq]        f32 (written)
+ *   softmax_scale must be finite and > 0.
+ *   bf16: d must be 64 or 128; runs on the tcgen05 tensor cores with fp32
+ *   accumulation (P is rounded to bf16 before P v).
+ *   f32: 4 <= d <= 128, d % 4 == 0; runs an exact fp32 SIMT kernel.
+ */
+int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out,
+                      const bea_tensor* lse, float softmax_scale, int is_causal, int window_left,
+                      int window_right, void* stream);
+
+/*
+ * Bytes of device workspace bea_flash_mha_bwd needs for q of shape
+ * [n, lq, h, d] (an fp32 dQ accumulator plus two fp32 values per row).
+ */
+size_t bea_flash_mha_bwd_workspace_size(int64_t n, int64_t lq, int64_t h, int64_t d);
+
+/*
+ * Backward from the GIVEN out and lse (picotron context_parallel.py,
+ * ring_attention_backward, Steps 1-6):
+ *   P = exp(softmax_scale * q k^T - lse) (masked entries 0), dV = P^T dO,
+ *   dP = dO v^T, D = rowsum(dO * out), dS = P * (dP - D),
+ *   dQ = softmax_scale * dS k, dK = softmax_scale * dS^T q,
+ * with dK, dV summed over the query heads of each K/V head. Using the final
+ * out/lse of the full row (not a chunk's) is what lets ring chunk pairs add
+ * their partial gradients (flash_sharding.py, "Ring Backward").
+ *
+ *   dout        [n, lq, h, d]    q's dtype
+ *   q, k, v     as for the forward
+ *   out         [n, lq, h, d]    q's dtype, or f32
+ *   lse         [n, h, lq]       f32
+ *   dq          [n, lq, h, d]    q's dtype or f32 (written)
+ *   dk, dv      [n, lk, h_kv, d] q's dtype or f32 (written)
+ *   accumulate  0: dq/dk/dv are overwritten; 1: the gradients are ADDED to
+ *               dq/dk/dv, which must then all be f32 (ring chunk pairs).
+ *   workspace   device buffer of at least bea_flash_mha_bwd_workspace_size()
+ *               bytes, 256-byte aligned, owned by the caller, contents on
+ *               entry irrelevant; calls that may run concurrently need
+ *               separate workspaces.
+ */
+int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k, const bea_tensor* v,
+                      const bea_tensor* out, const bea_tensor* lse, const bea_tensor* dq, const bea_tensor* dk,
+                      const bea_tensor* dv, float softmax_scale, int is_causal, int window_left,
+                      int window_right, int accumulate, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * Log-sum-exp merge, in place on the accumulator (flash_attn_jax
+ * flash_sharding.py, "Ring Forward"; the same fold as picotron
+ * update_out_and_lse in its sigmoid form). Per row r = (b, i, head):
+ *   M = max(La, Lb); if M == -inf the row is left unchanged; otherwise
+ *   L = M + log1p(exp(min(La, Lb) - M)), Oa <- exp(La - L) Oa + exp(Lb - L) Ob,
+ *   La <- L.
+ *
+ *   out_acc   [n, l, h, d] f32 (read and written)
+ *   lse_acc   [n, h, l]    f32 (read and written)
+ *   out_blk   [n, l, h, d] bf16 or f32
+ *   lse_blk   [n, h, l]    f32
+ *   out_final NULL, or [n, l, h, d] bf16: also receives the merged rows cast
+ *             to bf16 (the last step of a ring).
+ *   d must be 16, 32, 64 or 128.
+ */
+int bea_ring_merge(const bea_tensor* out_acc, const bea_tensor* lse_acc, const bea_tensor* out_blk,
+                   const bea_tensor* lse_blk, const bea_tensor* out_final, void* stream);
+
+/*
+ * Synchronises `stream`, reads the device status word of the current device
+ * and clears it. Returns BEA_OK, BEA_ERR_TIMEOUT if any kernel since the last
+ * read gave up a wait, BEA_ERR_UNSUPPORTED if a kernel met a configuration it
+ * cannot run, or BEA_ERR_CUDA.
+ */
+int bea_get_device_status(void* stream);
+
+/* Static English text for a status code. */
+const char* bea_status_string(int code);
+
+/* BEA_VERSION of the built library. */
+int bea_version(void);
+
+/*
+ * Failure-detection self test: launches one CTA whose thread waits on an
+ * mbarrier that nothing arrives on, with a limit of `limit_us` microseconds
+ * (1..2000000). The wait gives up, the kernel returns normally and the
+ * status word reads BEA_ERR_TIMEOUT afterwards. No trap, no fault.
+ */
+int bea_selftest_wait_timeout(int limit_us, void* stream);
+
+/* Number of kernels the last successful call on this host thread launched. */
+int bea_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEA_H_ */
