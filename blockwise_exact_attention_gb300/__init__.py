@@ -1,0 +1,22 @@
+"""Blockwise exact attention on GB300 (sm_103a).
+
+Public API (all calls run in libbea.so's CUDA kernels on the current stream):
+
+* ``flash_mha_fwd(q, k, v, softmax_scale, is_causal, window_size) -> (out, lse)``
+* ``flash_mha_bwd(dout, q, k, v, out, lse, ...) -> (dq, dk, dv)``
+* ``ring_merge(out_acc, lse_acc, out_blk, lse_blk, out_final=None)``
+* ``ring_attention_fwd / ring_attention_bwd``: ring attention replayed as
+  chunk steps on one GPU.
+
+The seeded input generators live in ``workloads`` and import nothing else.
+"""
+from .ops import (  # noqa: F401
+    bwd_workspace_bytes,
+    device_status,
+    flash_mha_bwd,
+    flash_mha_fwd,
+    launches_since_reset,
+    ring_merge,
+    selftest_wait_timeout,
+)
+from .ring import chunk_schedule, ring_attention_bwd, ring_attention_fwd  # noqa: F401

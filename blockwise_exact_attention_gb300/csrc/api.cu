@@ -69,7 +69,9 @@ int64_t numel(const bea_tensor* t) {
 }
 
 // Structural checks of one tensor: rank, dtype, non-negative shape/strides,
-// contiguous last dim, 16-byte aligned base and strides (when non-empty).
+// contiguous last dim, and (when non-empty) a base pointer and outer strides
+// aligned to `align` bytes: 16 for [n,l,h,d] tensors (TMA and vector
+// accesses), 4 for [n,h,l] log-sum-exp tensors (scalar accesses).
 int check_tensor(const bea_tensor* t, int ndim) {
   if (t == nullptr) return BEA_ERR_ARG;
   if (t->ndim != ndim) return BEA_ERR_SHAPE;
@@ -81,10 +83,11 @@ int check_tensor(const bea_tensor* t, int ndim) {
   if (numel(t) == 0) return BEA_OK;
   if (t->data == nullptr) return BEA_ERR_ARG;
   const int64_t es = esize(t->dtype);
+  const int64_t align = (ndim == 4) ? 16 : es;
   if (t->shape[ndim - 1] > 1 && t->stride[ndim - 1] != 1) return BEA_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return BEA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(t->data) % align != 0) return BEA_ERR_ALIGN;
   for (int i = 0; i < ndim - 1; ++i)
-    if (t->shape[i] > 1 && (t->stride[i] * es) % 16 != 0) return BEA_ERR_ALIGN;
+    if (t->shape[i] > 1 && (t->stride[i] * es) % align != 0) return BEA_ERR_ALIGN;
   return BEA_OK;
 }
 

@@ -1,0 +1,119 @@
+"""Ring attention replayed on one GPU as sequential chunk steps.
+
+The sequence is split into ``n_chunks`` equal chunks. In ring attention the
+device owning query chunk i holds, at step t, the K/V chunk that started on
+device i - t (ppermute sends i -> i+1). With causal masking the step's chunk
+pair is skipped when j > i, computed with the causal kernel on the diagonal
+j == i and with the full kernel otherwise; every computed block is folded into
+a running fp32 (out, lse) by the log-sum-exp merge (flash_attn_jax
+flash_sharding.py, sections "Ring Forward" and "Ring Backward").
+
+On one GPU the K/V "rotation" is a zero-copy chunk view of the resident
+tensors, so the schedule reduces to a sequence of forward calls and merges,
+all through the C ABI. The backward runs every visible chunk pair once with
+the final out/lse of its query rows and adds the partial gradients in fp32.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import ops
+
+
+def chunk_schedule(n_chunks: int, is_causal: bool):
+    """Per query chunk i: the ring steps [(t, j, kind)], kind in skip/causal/full."""
+    sched = []
+    for i in range(n_chunks):
+        steps = []
+        for t in range(n_chunks):
+            j = (i - t) % n_chunks
+            if not is_causal:
+                kind = "full"
+            elif j > i:
+                kind = "skip"
+            elif j == i:
+                kind = "causal"
+            else:
+                kind = "full"
+            steps.append((t, j, kind))
+        sched.append(steps)
+    return sched
+
+
+def _chunks(x, n_chunks, dim):
+    c = x.shape[dim] // n_chunks
+    return [x.narrow(dim, i * c, c) for i in range(n_chunks)]
+
+
+def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=True, out_dtype=None,
+                       block_dtype=None):
+    """Forward over ring chunk steps -> (out, lse).
+
+    ``out_dtype`` fp32 makes the fp32 accumulator itself the result;
+    otherwise (default: q's dtype) the last merge of each query chunk also
+    writes the cast result. ``block_dtype`` is the dtype of each block's
+    partial output (default: q's dtype, as the pages feed the kernel's
+    q-dtype output into the fp32 merge).
+    """
+    n, l, h, d = q.shape
+    if l % n_chunks:
+        raise ValueError("sequence length must split evenly into chunks")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    out_dtype = out_dtype or q.dtype
+    block_dtype = block_dtype or q.dtype
+    dev = q.device
+    out = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    lse = torch.empty((n, h, l), dtype=torch.float32, device=dev)
+    acc = out if out_dtype == torch.float32 else torch.empty(q.shape, dtype=torch.float32, device=dev)
+    c = l // n_chunks
+    qs, ks, vs = _chunks(q, n_chunks, 1), _chunks(k, n_chunks, 1), _chunks(v, n_chunks, 1)
+    accs, outs, lses = _chunks(acc, n_chunks, 1), _chunks(out, n_chunks, 1), _chunks(lse, n_chunks, 2)
+    blk = torch.empty((n, c, h, d), dtype=block_dtype, device=dev)
+    lse_blk = torch.empty((n, h, c), dtype=torch.float32, device=dev)
+    for i, steps in enumerate(chunk_schedule(n_chunks, is_causal)):
+        live = [(t, j, kind) for (t, j, kind) in steps if kind != "skip"]
+        for s, (_t, j, kind) in enumerate(live):
+            causal = kind == "causal"
+            last = s == len(live) - 1
+            if s == 0:
+                # the first block initialises the accumulator (merge with (0, -inf) is the identity)
+                target = outs[i] if (last and out_dtype != torch.float32) else accs[i]
+                ops.flash_mha_fwd(qs[i], ks[j], vs[j], softmax_scale, causal, out=target, lse=lses[i])
+            else:
+                ops.flash_mha_fwd(qs[i], ks[j], vs[j], softmax_scale, causal, out=blk, lse=lse_blk)
+                fin = outs[i] if (last and out_dtype != torch.float32) else None
+                ops.ring_merge(accs[i], lses[i], blk, lse_blk, out_final=fin)
+    return out, lse
+
+
+def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=None, is_causal=True):
+    """Backward over every visible chunk pair -> fp32 (dq, dk, dv)."""
+    n, l, h, d = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    if not is_causal:
+        dq.zero_()
+        dk.zero_()
+        dv.zero_()
+    ws = torch.empty(ops.bwd_workspace_bytes(_chunks(q, n_chunks, 1)[0]), dtype=torch.uint8, device=dev)
+    qs, ks, vs = _chunks(q, n_chunks, 1), _chunks(k, n_chunks, 1), _chunks(v, n_chunks, 1)
+    dos, os_, ls = _chunks(dout, n_chunks, 1), _chunks(out, n_chunks, 1), _chunks(lse, n_chunks, 2)
+    dqs, dks, dvs = _chunks(dq, n_chunks, 1), _chunks(dk, n_chunks, 1), _chunks(dv, n_chunks, 1)
+    for i, steps in enumerate(chunk_schedule(n_chunks, is_causal)):
+        for _t, j, kind in steps:
+            if kind == "skip":
+                continue
+            # causal, query chunks in ascending order: the diagonal pair (i, i) is the
+            # first to touch dq_i, dk_i and dv_i, so it overwrites instead of adding
+            first = is_causal and kind == "causal"
+            ops.flash_mha_bwd(dos[i], qs[i], ks[j], vs[j], os_[i], ls[i], softmax_scale, kind == "causal",
+                              dq=dqs[i], dk=dks[j], dv=dvs[j], accumulate=not first, workspace=ws)
+    return dq, dk, dv

@@ -16,7 +16,8 @@
  *   aligned and the other strides multiples of 16 bytes, so that chunk views
  *   of a longer sequence (an offset base pointer with the parent's strides)
  *   are accepted without a copy. The log-sum-exp is [n, h, l] fp32, natural
- *   log, softmax_scale included, with a contiguous last dimension
+ *   log, softmax_scale included, with a contiguous last dimension and
+ *   4-byte alignment
  *   (flash_attn_jax flash_sharding.py, sections "Sharding" and "Ring
  *   Forward": out [n,l,h,d], lse [n,h,l]).
  *
