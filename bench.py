@@ -1,0 +1,372 @@
+"""Benchmark: attention TFLOP/s, forward and forward+backward, bf16 causal.
+
+Workload: causal GQA, q [1, 8192, 32, 128], k/v [1, 8192, 8, 128] (group 4),
+rotary embedding applied on the host, softmax_scale 1/sqrt(128) — the causal
+bf16 L=8192 d=128 configuration the throughput target is quoted on. One step
+is the whole hot path on one batch: the forward (O and the log-sum-exp) and
+the backward recomputed from it (D/lse preprocess, the tcgen05 main kernel,
+dQ convert). Algorithmic FLOPs: 4*n*h*l^2*d/2 forward, 2.5x that backward.
+
+Besides the headline line it reports, in the same JSON line: the ring_merge
+kernel standalone on [1, 16384, 16, 128] (fp32 accumulator, bf16 block; GB/s
+of algorithmic bytes, L2 flushed), the ring replay of the 16k causal workload
+(8 chunks), the end-to-end number through the public API with host buffers,
+and the fp64 CPU oracle on a bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 it runs under torchrun, one independent replica per GPU (the path
+does not shard): value = all replicas' FLOPs / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, causal) and % of GB300 BF16 tensor peak"
+WORKLOAD = "causal_gqa_8k_rope"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def bench_config(world: int) -> dict:
+    return {"workload": "causal GQA bf16 q[1,8192,32,128] k/v[1,8192,8,128], RoPE on host, scale 1/sqrt(128)",
+            "global_batch": world, "seq_len": 8192, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (~300 MB per step) and a 256 MB L2 flush before every step"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bea_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (the reference arm and the cpu_baseline field)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(x, w, heads_kv):
+    """fwd + bwd of the fp64 oracle on the query heads of `heads_kv`; returns FLOPs done."""
+    import numpy as np
+    import oracle
+    g = w.h // w.h_kv
+    hqs = [kv * g + t for kv in heads_kv for t in range(g)]
+    q, k, v, do = x["q"][:, :, hqs], x["k"][:, :, heads_kv], x["v"][:, :, heads_kv], x["dout"][:, :, hqs]
+    out, lse = oracle.attention_fwd(q, k, v, w.softmax_scale, w.is_causal, w.window)
+    oracle.attention_bwd(do, q, k, v, out.astype(np.float32), lse, w.softmax_scale, w.is_causal, w.window)
+    f, b = oracle.algorithmic_flops(w.n, len(hqs), w.l, w.l, w.d, w.is_causal, w.window)
+    return f + b
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from blockwise_exact_attention_gb300 import workloads
+    w = workloads.WORKLOADS[WORKLOAD]
+    x = workloads.make_inputs(w)
+    for _ in range(max(0, args.warmup)):
+        oracle_sample_step(x, w, [0])
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = oracle_sample_step(x, w, [0])
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    val = flops / sec / 1e12
+    sample = (f"K/V head 0 of {w.h_kv} (query heads 0..{w.h // w.h_kv - 1}), all 8192 rows, fwd+bwd in fp64 numpy; "
+              f"{flops:.3e} algorithmic FLOPs per step")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": bench_config(args.gpus),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import __graft_entry__ as ge
+    ge.build()
+    import oracle
+    import blockwise_exact_attention_gb300 as bea
+    from blockwise_exact_attention_gb300 import workloads
+
+    pk_burst, pk_sust, pk_hbm, pk_kind = peaks()
+    w = workloads.WORKLOADS[WORKLOAD]
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda", local)
+    q, k, v, do = (torch.from_numpy(x[s]).to(dev).to(torch.bfloat16) for s in ("q", "k", "v", "dout"))
+    s = w.softmax_scale
+    out = torch.empty_like(q)
+    lse = torch.empty((w.n, w.h, w.l), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(bea.bwd_workspace_bytes(q), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    f_fwd, f_bwd = oracle.algorithmic_flops(w.n, w.h, w.l, w.l, w.d, w.is_causal, w.window)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        bea.flash_mha_fwd(q, k, v, s, True, out=out, lse=lse)
+
+    def bwd():
+        bea.flash_mha_bwd(do, q, k, v, out, lse, s, True, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def timed(fn, reps, warm):
+        for _ in range(warm):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return ts
+
+    # ---- headline: K steps of fwd + bwd, each step timed between L2 flushes ----
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    bea.launches_since_reset(reset=True)
+    t_fwd, t_bwd = [], []
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            fwd()
+            e1.record(stream)
+            bwd()
+            e2.record(stream)
+            e2.synchronize()
+            t_fwd.append(e0.elapsed_time(e1))
+            t_bwd.append(e1.elapsed_time(e2))
+        torch.cuda.synchronize()
+    launches = bea.launches_since_reset(reset=True)
+    status = bea.device_status()
+    ms_fwd = sum(t_fwd) / len(t_fwd)
+    ms_bwd = sum(t_bwd) / len(t_bwd)
+    ms_step = ms_fwd + ms_bwd
+    if dist:
+        tt = torch.tensor([ms_step, ms_fwd, ms_bwd], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, ms_fwd, ms_bwd = (float(v_) for v_ in tt)
+    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    fwd_tf = f_fwd / (ms_fwd * 1e-3) / 1e12
+    bwd_tf = f_bwd / (ms_bwd * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ----
+    hq_, hk_, hv_, hdo_ = (t.cpu().pin_memory() for t in (q, k, v, do))
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h_dq, h_dk, h_dv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hdo_))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_dq, h_dk, h_dv))
+
+    def e2e_step():
+        q.copy_(hq_, non_blocking=True)
+        k.copy_(hk_, non_blocking=True)
+        v.copy_(hv_, non_blocking=True)
+        do.copy_(hdo_, non_blocking=True)
+        fwd()
+        bwd()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        h_dq.copy_(dq, non_blocking=True)
+        h_dk.copy_(dk, non_blocking=True)
+        h_dv.copy_(dv, non_blocking=True)
+
+    e2e_ms = statistics.mean(timed(e2e_step, max(3, args.steps // 4), 2))
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt[0])
+    e2e_val = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    # ---- ring_merge standalone, [1, 16384, 16, 128], L2 flushed ----
+    wr = workloads.WORKLOADS["ring_causal_16k"]
+    acc = torch.randn((1, wr.l, wr.h, wr.d), device=dev)
+    lacc = torch.randn((1, wr.h, wr.l), device=dev)
+    blk = torch.randn((1, wr.l, wr.h, wr.d), device=dev).to(torch.bfloat16)
+    lblk = torch.randn((1, wr.h, wr.l), device=dev)
+    merge_ms = statistics.median(timed(lambda: bea.ring_merge(acc, lacc, blk, lblk), 20, 3))
+    rows = wr.n * wr.l * wr.h
+    merge_bytes = rows * (wr.d * (4 + 4 + 2) + 12)
+    merge_gbs = merge_bytes / (merge_ms * 1e-3) / 1e9
+
+    # ---- ring replay of the 16k causal workload, 8 chunks ----
+    qr = torch.randn((1, wr.l, wr.h, wr.d), device=dev).to(torch.bfloat16)
+    kr = torch.randn_like(qr)
+    vr = torch.randn_like(qr)
+    ring_ms = statistics.median(timed(lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True),
+                                      5, 2))
+    rf, _ = oracle.algorithmic_flops(1, wr.h, wr.l, wr.l, wr.d, True)
+    single_ms = statistics.median(timed(lambda: bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True), 5, 2))
+    del qr, kr, vr, acc, lacc, blk, lblk
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        fl = oracle_sample_step(x, w, [0])
+        sec = time.perf_counter() - t0
+        cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fwd+bwd of K/V head 0 (query heads 0..3) of the same workload, all rows, fp64 numpy, "
+                         f"{fl:.3e} FLOPs in {sec:.1f} s"}
+
+    bwd_launch_ms = ms_bwd
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": bench_config(world),
+        "fwd_tflops": fwd_tf,
+        "bwd_tflops": bwd_tf,
+        "ms_fwd": ms_fwd,
+        "ms_bwd": ms_bwd,
+        "pct_peak": {"fwd": fwd_tf / pk_burst, "bwd": bwd_tf / pk_burst, "fwd_bwd": value / world / pk_burst,
+                     "peak_tflops": pk_burst, "peak_kind": f"{pk_kind} bf16 burst"},
+        "roofline": {"bound": "tensor", "kernel": "bwd (preprocess + tcgen05 main + dQ convert, one call)",
+                     "achieved": bwd_tf, "peak": pk_burst, "unit": "TFLOP/s", "frac": bwd_tf / pk_burst,
+                     "traffic": None, "peak_kind": f"{pk_kind} bf16 burst (kernel timed alone per step)"},
+        "roofline_fwd": {"bound": "tensor", "kernel": "fwd_bf16_kernel<128>", "achieved": fwd_tf, "peak": pk_burst,
+                         "unit": "TFLOP/s", "frac": fwd_tf / pk_burst, "traffic": None},
+        "merge": {"kernel": "ring_merge [1,16384,16,128] f32 acc + bf16 blk", "ms": merge_ms,
+                  "bytes": merge_bytes, "gbs": merge_gbs, "peak_gbs": pk_hbm, "frac": merge_gbs / pk_hbm},
+        "ring": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks (36 fwd + 28 merges)", "ms": ring_ms,
+                 "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "device_status": status,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -291,7 +291,35 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
                         seq4(dv), lse3(lse),  reinterpret_cast<float*>(ws + w.d_off), accumulate};
     return finish(bea::launch_bwd_f32(p, s, &launches), launches);
   }
-  return BEA_ERR_UNSUPPORTED;
+  bea::BwdParams p;
+  p.a = a;
+  p.dout = seq4(dout);
+  p.out = seq4(out);
+  p.dq = seq4(dq);
+  p.dk = seq4(dk);
+  p.dv = seq4(dv);
+  p.out_is_f32 = out->dtype == BEA_F32;
+  p.dq_is_f32 = dq->dtype == BEA_F32;
+  p.dk_is_f32 = dk->dtype == BEA_F32;
+  p.dv_is_f32 = dv->dtype == BEA_F32;
+  p.lse = lse3(lse);
+  p.accumulate = accumulate;
+  p.dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
+  p.d_row = reinterpret_cast<float*>(ws + w.d_off);
+  p.lse2 = reinterpret_cast<float*>(ws + w.l_off);
+  p.lq_pad = (a.lq + 127) / 128 * 128;
+  if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  std::memset(&tq, 0, sizeof(tq));
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  std::memset(&tdo, 0, sizeof(tdo));
+  if (a.lq > 0 && a.lk > 0) {
+    if ((rc = make_seq_map(q, &tq)) || (rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv)) ||
+        (rc = make_seq_map(dout, &tdo)))
+      return rc;
+  }
+  return finish(bea::launch_bwd_bf16(p, tq, tk, tv, tdo, s, &launches), launches);
 }
 
 int bea_ring_merge(const bea_tensor* out_acc, const bea_tensor* lse_acc, const bea_tensor* out_blk,

@@ -1,0 +1,580 @@
+// Attention backward on sm_103a tensor cores, recomputed from the log-sum-exp.
+//
+// picotron context_parallel.py, ring_attention_backward, Steps 1-6:
+//   P = exp(scale Q K^T - L)  (masked entries 0)
+//   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q,
+// with dK, dV summed over the query heads that share a K/V head
+// (RingAttention._repeat_kv read backwards). O and L are the caller's, not
+// recomputed, so partial gradients of ring chunk pairs add up exactly.
+//
+// Three launches:
+//   1. preprocess: D and L*log2(e) per query row into the workspace (padding
+//      rows get D = 0, L2 = +inf so that their P is exactly 0), and the fp32
+//      dQ accumulator rows zeroed;
+//   2. main: one CTA per (128-key block, batch, K/V head). K and V stay in
+//      shared memory; the CTA walks the group's query heads x the 128-row
+//      query tiles the causal/window band lets it see:
+//        warp 8      TMA producer (K, V once; Q_i and dO_i into 2 stages),
+//        warp 9      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM,
+//                    then dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i and
+//                    dQ_i = dS K (dS^T from shared memory, read K-major for
+//                    dK and MN-major for dQ),
+//        warps 0-3   one thread per key: P^T and dS^T from S^T, dP^T, L2, D;
+//                    finally the dK/dV epilogue,
+//        warps 4-7   one thread per query row: move dQ_i out of TMEM and
+//                    bulk-reduce-add it (fp32) into the workspace.
+//      dK and dV accumulate in TMEM across the whole group: no atomics.
+//   3. convert: dQ = scale * accumulator, cast or added into the caller's dq.
+//
+// TMEM (512 columns): S^T [0,128) (P^T packed bf16 over its first 64
+// columns), dP^T [128,256) (later dQ_i), dV [256,256+D), dK [384,384+D).
+//
+// Workspace dQ accumulator layout (fp32): per (b, head, 128-row query tile),
+// D/64 blocks of [128 rows x 64 columns]; inside a row, 16-byte chunk c is
+// stored at position c ^ (row & 15) so that the staging writes of a warp hit
+// distinct shared-memory banks. Every block is one contiguous 32 KB bulk
+// reduce.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace bea {
+namespace {
+
+constexpr int kBM = 128;  // query rows per iteration
+constexpr int kBN = 128;  // keys per CTA
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kDrainBar = 1;  // named barrier of the drain warpgroup
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;          // 2 stages
+  static constexpr int kDOOff = kQOff + 2 * kTileBytes;     // 2 stages
+  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;    // dS^T [128 keys x 128 q] bf16, also dQ staging
+  static constexpr int kDSBytes = 128 * 128 * 2;
+  static constexpr int kBarOff = kDSOff + kDSBytes;
+  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 6 + 1;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort, drain verdict*/ + 1024;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+  static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, false, true);     // dV (TMEM A), dK
+  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true, true);       // dQ
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ float* dq_acc_tile(const BwdParams& p, int b, int hq, int qt) {
+  const int nqt = p.lq_pad / kBM;
+  return p.dq_acc + ((size_t)(b * p.a.h + hq) * nqt + qt) * (size_t)(kBM * p.a.d);
+}
+
+// ---------------------------------------------------------------------------
+// 1. preprocess
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdParams p) {
+  const AttnDims& a = p.a;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // over n * h * lq_pad
+  const int64_t total = (int64_t)a.n * a.h * p.lq_pad;
+  if (row >= total) return;
+  const int i = (int)(row % p.lq_pad);
+  const int bh = (int)(row / p.lq_pad);
+  const int hq = bh % a.h, b = bh / a.h;
+  float dsum = 0.f, l2 = INFINITY;
+  if (i < a.lq) {
+    const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout.ptr) + b * p.dout.sn +
+                             (int64_t)i * p.dout.sl + hq * p.dout.sh;
+    for (int c = lane * 4; c < a.d; c += 128) {
+      const uint2 graw = *reinterpret_cast<const uint2*>(g + c);
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
+      float4 o;
+      if (p.out_is_f32) {
+        o = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out.ptr) + b * p.out.sn +
+                                             (int64_t)i * p.out.sl + hq * p.out.sh + c);
+      } else {
+        const uint2 oraw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.out.ptr) +
+                                                           b * p.out.sn + (int64_t)i * p.out.sl + hq * p.out.sh + c);
+        const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&oraw.x));
+        const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&oraw.y));
+        o = make_float4(o01.x, o01.y, o23.x, o23.y);
+      }
+      dsum = fmaf(g01.x, o.x, dsum);
+      dsum = fmaf(g01.y, o.y, dsum);
+      dsum = fmaf(g23.x, o.z, dsum);
+      dsum = fmaf(g23.y, o.w, dsum);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    const float L = p.lse.ptr[b * p.lse.sn + hq * p.lse.sh + i];
+    if (L != -INFINITY) l2 = L * 1.4426950408889634f;
+  }
+  if (lane == 0) {
+    p.d_row[row] = (i < a.lq) ? dsum : 0.f;
+    p.lse2[row] = l2;
+  }
+  // zero this row of the dQ accumulator (D/64 blocks of 64 floats, contiguous per block)
+  float* tile = dq_acc_tile(p, b, hq, i / kBM);
+  const int r = i % kBM;
+  for (int c = lane * 4; c < a.d; c += 128) {
+    const int blk = c / 64, cc = c % 64;
+    *reinterpret_cast<float4*>(tile + (size_t)blk * kBM * 64 + r * 64 + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. convert
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) bwd_convert_dq_kernel(BwdParams p) {
+  const AttnDims& a = p.a;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // over n * h * lq
+  const int64_t total = (int64_t)a.n * a.h * a.lq;
+  if (row >= total) return;
+  const int i = (int)(row % a.lq);
+  const int bh = (int)(row / a.lq);
+  const int hq = bh % a.h, b = bh / a.h;
+  const float* tile = dq_acc_tile(p, b, hq, i / kBM);
+  const int r = i % kBM;
+  for (int c = lane * 4; c < a.d; c += 128) {
+    const int blk = c / 64, chunk = (c % 64) / 4;
+    const int phys = chunk ^ (r & 15);
+    float4 v = *reinterpret_cast<const float4*>(tile + (size_t)blk * kBM * 64 + r * 64 + phys * 4);
+    v.x *= a.scale;
+    v.y *= a.scale;
+    v.z *= a.scale;
+    v.w *= a.scale;
+    if (p.dq_is_f32) {
+      float* dst = reinterpret_cast<float*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
+      if (p.accumulate) {
+        const float4 o = *reinterpret_cast<const float4*>(dst);
+        v.x += o.x;
+        v.y += o.y;
+        v.z += o.z;
+        v.w += o.w;
+      }
+      *reinterpret_cast<float4*>(dst) = v;
+    } else {
+      __nv_bfloat16* dst =
+          reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
+      uint2 raw;
+      raw.x = pack_bf16x2(v.x, v.y);
+      raw.y = pack_bf16x2(v.z, v.w);
+      *reinterpret_cast<uint2*>(dst) = raw;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+
+struct BwdSched {
+  int k0;          // first key of the block
+  int i_lo, i_hi;  // visible query tiles
+  int g;           // query heads per K/V head
+  int n_iter;      // g * (i_hi - i_lo)
+};
+
+__device__ __forceinline__ bool bwd_tile_needs_mask(const AttnDims& a, int k0, int q0) {
+  if (k0 + kBN - 1 >= a.lk) return true;
+  if (a.wl >= 0 && k0 < q0 + kBM - 1 - a.wl) return true;
+  if (a.wr >= 0 && k0 + kBN - 1 > q0 + a.wr) return true;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const BwdParams p, float scale_log2) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* do_full = q_full + 2;
+  uint64_t* qdo_empty = do_full + 2;
+  uint64_t* sp_full = qdo_empty + 2;
+  uint64_t* ds_ready = sp_full + 1;
+  uint64_t* dq_full = ds_ready + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* ds_free = dq_empty + 1;
+  uint64_t* dkv_full = ds_free + 1;
+  uint64_t* mma_done = dkv_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const AttnDims& a = p.a;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // ---- work: key blocks in ascending order (under a causal mask the first see the most queries) ----
+  const int nkv = a.n * a.hkv;
+  const int kb = blockIdx.x / nkv;
+  const int b = (blockIdx.x % nkv) / a.hkv;
+  const int kvh = (blockIdx.x % nkv) % a.hkv;
+  BwdSched sc;
+  sc.k0 = kb * kBN;
+  sc.g = a.h / a.hkv;
+  {
+    const int k1 = min(sc.k0 + kBN, a.lk) - 1;
+    const int qmin = (a.wr < 0) ? 0 : max(0, sc.k0 - a.wr);
+    const int qmax = (a.wl < 0) ? a.lq : min(a.lq, k1 + a.wl + 1);
+    if (qmax > qmin) {
+      sc.i_lo = qmin / kBM;
+      sc.i_hi = (qmax + kBM - 1) / kBM;
+    } else {
+      sc.i_lo = sc.i_hi = 0;
+    }
+    sc.n_iter = sc.g * (sc.i_hi - sc.i_lo);
+  }
+  const int nt = sc.i_hi - sc.i_lo;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&do_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ds_ready, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(ds_free, 1);
+    mbar_init(dkv_full, 1);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384;
+
+  if (warp == kProducerWarp) {
+    // ========================== TMA producer ==========================
+    if (lane == 0 && sc.n_iter > 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+      for (int x = 0; x < C::kBoxes; ++x) {
+        tma_load_4d(smem + C::kKOff + x * 16384, &tk, kv_full, x * 64, kvh, sc.k0, b);
+        tma_load_4d(smem + C::kVOff + x * 16384, &tv, kv_full, x * 64, kvh, sc.k0, b);
+      }
+      int it = 0;
+      for (; it < sc.n_iter; ++it) {
+        const int s = it & 1;
+        const int hq = kvh * sc.g + it / nt;
+        const int q0 = (sc.i_lo + it % nt) * kBM;
+        if (it >= 2 && !wait_parity(&qdo_empty[s], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kQOff + s * C::kTileBytes + x * 16384, &tq, &q_full[s], x * 64, hq, q0, b);
+        mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kDOOff + s * C::kTileBytes + x * 16384, &tdo, &do_full[s], x * 64, hq, q0, b);
+      }
+      // loads still in flight must land before shared memory goes away
+      volatile int no_abort = 0;
+      wait_parity(kv_full, 0, &no_abort, p.status, 200000000ull);
+      for (int k = max(0, it - 2); k < it; ++k) {
+        wait_parity(&q_full[k & 1], (k >> 1) & 1, &no_abort, p.status, 200000000ull);
+        wait_parity(&do_full[k & 1], (k >> 1) & 1, &no_abort, p.status, 200000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ========================== MMA issuer ==========================
+    if (lane == 0) {
+      const uint32_t k_addr = smem_u32(smem + C::kKOff);
+      const uint32_t v_addr = smem_u32(smem + C::kVOff);
+      const uint32_t ds_addr = smem_u32(smem + C::kDSOff);
+      bool ok = sc.n_iter > 0 && wait_parity(kv_full, 0, abort_flag, p.status);
+      for (int it = 0; ok && it < sc.n_iter; ++it) {
+        const int s = it & 1;
+        const uint32_t par = (it >> 1) & 1;
+        const uint32_t q_addr = smem_u32(smem + C::kQOff + s * C::kTileBytes);
+        const uint32_t do_addr = smem_u32(smem + C::kDOOff + s * C::kTileBytes);
+        if (!(ok = wait_parity(&q_full[s], par, abort_flag, p.status))) break;
+        tc_fence_after();
+        // S^T = K Q^T   (M = keys, N = queries, K = d; both K-major)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          umma_ss(tmem + T_S, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024), C::kIdescS,
+                  k > 0 ? 1u : 0u);
+        }
+        if (it > 0 && !(ok = wait_parity(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
+        if (!(ok = wait_parity(&do_full[s], par, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dP^T = V dO^T
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          umma_ss(tmem + T_DP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
+                  C::kIdescS, k > 0 ? 1u : 0u);
+        }
+        umma_commit(sp_full);
+        if (!(ok = wait_parity(ds_ready, it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dV += P^T dO    (A = P^T from TMEM, B = dO MN-major)
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k)
+          umma_ts(tmem + T_DV, tmem + T_S + k * 8, sdesc_sw128(do_addr + k * 2048, 16384, 1024), C::kIdescKV,
+                  (it > 0 || k > 0) ? 1u : 0u);
+        // dK += dS^T Q    (A = dS^T K-major, B = Q MN-major)
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          umma_ss(tmem + T_DK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(q_addr + k * 2048, 16384, 1024),
+                  C::kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+        }
+        // dQ = dS K       (A = dS^T buffer read MN-major, B = K MN-major), into the dP^T columns
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          umma_ss(tmem + T_DP, sdesc_sw128(ds_addr + k * 2048, 16384, 1024), sdesc_sw128(k_addr + k * 2048, 16384, 1024),
+                  C::kIdescQ, k > 0 ? 1u : 0u);
+        umma_commit(dq_full);
+        umma_commit(&qdo_empty[s]);
+      }
+      if (ok && sc.n_iter > 0) umma_commit(dkv_full);
+      umma_commit(mma_done);
+      volatile int no_abort = 0;
+      wait_parity(mma_done, 0, &no_abort, p.status, 200000000ull);
+    }
+  } else if (warp < 4) {
+    // ========================== P^T / dS^T (one thread per key) ==========================
+    const int j = threadIdx.x;  // key row == TMEM lane
+    const int kj = sc.k0 + j;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t s_t = tmem + lane_base + T_S;
+    const uint32_t dp_t = tmem + lane_base + T_DP;
+    uint8_t* ds_row = smem + C::kDSOff + j * 128;
+    bool ok = true;
+    for (int it = 0; it < sc.n_iter; ++it) {
+      const int hq = kvh * sc.g + it / nt;
+      const int q0 = (sc.i_lo + it % nt) * kBM;
+      if (!(ok = wait_parity(sp_full, it & 1, abort_flag, p.status))) break;
+      if (it > 0 && !(ok = wait_parity(ds_free, (it - 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      const bool need_mask = bwd_tile_needs_mask(a, sc.k0, q0);
+      const float* l2 = p.lse2 + (size_t)(b * a.h + hq) * p.lq_pad + q0;
+      const float* dd = p.d_row + (size_t)(b * a.h + hq) * p.lq_pad + q0;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(s_t + cc * 32, sv);
+        tmem_ld32(dp_t + cc * 32, pv);
+        tmem_wait_ld();
+        reg_fence<32>(sv);
+        reg_fence<32>(pv);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 L4 = *reinterpret_cast<const float4*>(l2 + cc * 32 + e4 * 4);
+          const float4 D4 = *reinterpret_cast<const float4*>(dd + cc * 32 + e4 * 4);
+          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+          const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+          float pr[4], dsr[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = e4 * 4 + u;
+            float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, -Lv[u]));
+            if (need_mask) {
+              const int qi = q0 + cc * 32 + e;
+              if (!(kj < a.lk && key_visible(qi, kj, a.wl, a.wr))) pe = 0.f;
+            }
+            pr[u] = pe;
+            dsr[u] = pe * (__uint_as_float(pv[e]) - Dv[u]);
+          }
+          pk[e4 * 2] = pack_bf16x2(pr[0], pr[1]);
+          pk[e4 * 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+          dk[e4 * 2] = pack_bf16x2(dsr[0], dsr[1]);
+          dk[e4 * 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
+        }
+        // P^T (packed bf16 pairs) over the S^T columns already read
+        tmem_st16(s_t + cc * 16, pk);
+        // dS^T row j, queries [32cc, 32cc+32): 4 chunks of 16 B, 128-byte swizzle
+        uint8_t* half = ds_row + (cc >> 1) * 16384;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (cc & 1) * 4 + u;
+          const int phys = chunk ^ (j & 7);
+          *reinterpret_cast<uint4*>(half + phys * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(ds_ready);
+    }
+    // ---- dK / dV epilogue ----
+    if (ok && sc.n_iter > 0) ok = wait_parity(dkv_full, 0, abort_flag, p.status);
+    if (ok && kj < a.lk) {
+      tc_fence_after();
+      const bool have = sc.n_iter > 0;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t vv[32], kk[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + T_DV + c0, vv);
+          tmem_ld32(tmem + lane_base + T_DK + c0, kk);
+          tmem_wait_ld();
+          reg_fence<32>(vv);
+          reg_fence<32>(kk);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) vv[c] = kk[c] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) kk[c] = __float_as_uint(__uint_as_float(kk[c]) * a.scale);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t* src = which ? kk : vv;
+          const bool f32 = which ? p.dk_is_f32 : p.dv_is_f32;
+          void* base = which ? p.dk.ptr : p.dv.ptr;
+          const int64_t off = which ? (b * p.dk.sn + (int64_t)kj * p.dk.sl + kvh * p.dk.sh + c0)
+                                    : (b * p.dv.sn + (int64_t)kj * p.dv.sl + kvh * p.dv.sh + c0);
+          if (f32) {
+            float* dst = reinterpret_cast<float*>(base) + off;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              float4 v4 = make_float4(__uint_as_float(src[c]), __uint_as_float(src[c + 1]),
+                                      __uint_as_float(src[c + 2]), __uint_as_float(src[c + 3]));
+              if (p.accumulate) {
+                const float4 o = *reinterpret_cast<const float4*>(dst + c);
+                v4.x += o.x;
+                v4.y += o.y;
+                v4.z += o.z;
+                v4.w += o.w;
+              }
+              *reinterpret_cast<float4*>(dst + c) = v4;
+            }
+          } else {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + off;
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v4;
+              v4.x = pack_bf16x2(__uint_as_float(src[c]), __uint_as_float(src[c + 1]));
+              v4.y = pack_bf16x2(__uint_as_float(src[c + 2]), __uint_as_float(src[c + 3]));
+              v4.z = pack_bf16x2(__uint_as_float(src[c + 4]), __uint_as_float(src[c + 5]));
+              v4.w = pack_bf16x2(__uint_as_float(src[c + 6]), __uint_as_float(src[c + 7]));
+              *reinterpret_cast<uint4*>(dst + c) = v4;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ========================== dQ drain (one thread per query row) ==========================
+    const int r = threadIdx.x - 128;  // query row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const uint32_t dq_t = tmem + lane_base + T_DP;
+    uint8_t* stage = smem + C::kDSOff;
+    volatile int* drain_ok = abort_flag + 1;  // one thread waits, the group follows its verdict
+    for (int it = 0; it < sc.n_iter; ++it) {
+      const int hq = kvh * sc.g + it / nt;
+      const int qt = sc.i_lo + it % nt;
+      if (r == 0) *drain_ok = wait_parity(dq_full, it & 1, abort_flag, p.status) ? 1 : 0;
+      named_bar_sync(kDrainBar, 128);
+      if (!*drain_ok) break;
+      tc_fence_after();
+      uint32_t v[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(dq_t + c0, v + c0);
+      tmem_wait_ld();
+      reg_fence<D>(v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      float* dst = dq_acc_tile(p, b, hq, qt);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk) {
+        // the dS^T buffer is free: dK and dQ of this iteration have completed
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int phys = c ^ (r & 15);
+          *reinterpret_cast<uint4*>(stage + r * 256 + phys * 16) =
+              make_uint4(v[blk * 64 + 4 * c], v[blk * 64 + 4 * c + 1], v[blk * 64 + 4 * c + 2], v[blk * 64 + 4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(kDrainBar, 128);
+        if (r == 0) {
+          bulk_reduce_add_f32(dst + (size_t)blk * kBM * 64, stage, kBM * 64 * 4);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+        }
+        named_bar_sync(kDrainBar, 128);
+      }
+      if (r == 0) mbar_arrive(ds_free);
+    }
+    if (r == 0) bulk_wait_group<0>();
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
+  using C = BwdCfg<D>;
+  const AttnDims& a = p.a;
+  cudaError_t e;
+  {
+    const int64_t rows = (int64_t)a.n * a.h * p.lq_pad;
+    if (rows > 0) {
+      bwd_preprocess_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+      *nlaunch += 1;
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  const int nkb = (a.lk + kBN - 1) / kBN;
+  const long long blocks = (long long)nkb * a.n * a.hkv;
+  if (blocks > 0) {
+    e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const float scale_log2 = a.scale * 1.4426950408889634f;
+    bwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p, scale_log2);
+    *nlaunch += 1;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const int64_t qrows = (int64_t)a.n * a.h * a.lq;
+  if (qrows > 0) {
+    bwd_convert_dq_kernel<<<(unsigned)((qrows + 7) / 8), 256, 0, s>>>(p);
+    *nlaunch += 1;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
+  if (p.a.d == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, s, nlaunch);
+  if (p.a.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, s, nlaunch);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bea

@@ -72,6 +72,22 @@ struct FwdParams {
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, cudaStream_t s, int* nlaunch);
 
+struct BwdParams {
+  AttnDims a;
+  Seq4 dout, out, dq, dk, dv;
+  int out_is_f32, dq_is_f32, dk_is_f32, dv_is_f32;
+  Lse3 lse;
+  int accumulate;
+  float* dq_acc;  // workspace: fp32 dQ partial sums, tile-major (see bwd_sm103.cu)
+  float* d_row;   // workspace: [n, h, lq_pad] D = rowsum(dO * O)
+  float* lse2;    // workspace: [n, h, lq_pad] lse * log2(e), +inf for rows without keys / padding
+  int lq_pad;
+  uint32_t* status;
+};
+// Tensor maps over q, k, v, dout are built by the caller (api.cu).
+cudaError_t launch_bwd_bf16(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s, int* nlaunch);
+
 cudaError_t launch_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace bea
