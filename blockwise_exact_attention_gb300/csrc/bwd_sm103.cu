@@ -370,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < sc.n_iter; ++it) {
       const int hq = kvh * sc.g + it / nt;
       const int q0 = (sc.i_lo + it % nt) * kBM;
-      if (!(ok = wait_parity(sp_full, it & 1, abort_flag, p.status))) break;
-      if (it > 0 && !(ok = wait_parity(ds_free, (it - 1) & 1, abort_flag, p.status))) break;
+      if (!(ok = warp_wait_parity(sp_full, it & 1, abort_flag, p.status))) break;
+      if (it > 0 && !(ok = warp_wait_parity(ds_free, (it - 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
       const bool need_mask = bwd_tile_needs_mask(a, sc.k0, q0);
       const float* l2 = p.lse2 + (size_t)(b * a.h + hq) * p.lq_pad + q0;
@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(ds_ready);
     }
     // ---- dK / dV epilogue ----
-    if (ok && sc.n_iter > 0) ok = wait_parity(dkv_full, 0, abort_flag, p.status);
-    if (ok && kj < a.lk) {
+    if (ok && sc.n_iter > 0) ok = warp_wait_parity(dkv_full, 0, abort_flag, p.status);
+    if (ok) {
       tc_fence_after();
       const bool have = sc.n_iter > 0;
 #pragma unroll 1
@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < 32; ++c) kk[c] = __float_as_uint(__uint_as_float(kk[c]) * a.scale);
+        if (kj >= a.lk) continue;  // ragged last key block: loads above stay warp-wide
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t* src = which ? kk : vv;
@@ -527,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- teardown ----
+  __syncwarp();  // lane-0-only roles rejoin their warp before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {

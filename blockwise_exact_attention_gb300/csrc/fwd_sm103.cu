@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int it = 0;
     for (int j = sc.lo[t]; j < sc.hi[t]; ++j, ++it) {
-      if (!(ok = wait_parity(&s_full[t], it & 1, abort_flag, p.status))) break;
+      if (!(ok = warp_wait_parity(&s_full[t], it & 1, abort_flag, p.status))) break;
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld32(s_tmem + 0, sr);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue ----
     const bool have_o = sc.lo[t] < sc.hi[t];
-    if (ok && have_o) ok = wait_parity(&o_full[t], 0, abort_flag, p.status);
+    if (ok && have_o) ok = warp_wait_parity(&o_full[t], 0, abort_flag, p.status);
     if (ok && qs < a.lq) {
       tc_fence_after();
       const bool row_ok = qi < a.lq;
@@ -430,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- teardown ----
+  __syncwarp();  // lane-0-only roles rejoin their warp before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {

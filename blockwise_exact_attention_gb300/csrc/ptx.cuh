@@ -90,6 +90,15 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, vola
   }
 }
 
+// wait_parity() by every lane of a warp, with a warp-uniform verdict and the
+// warp reconverged afterwards (the .sync.aligned tcgen05 accesses that follow
+// need all 32 lanes together).
+__device__ __forceinline__ bool warp_wait_parity(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                 uint32_t* status) {
+  const bool ok = wait_parity(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
@@ -289,9 +298,12 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Named barrier among `nthreads` threads (a multiple of 32) of the CTA.
+// Named barrier among `nthreads` threads (a multiple of 32) of the CTA. The
+// warp is reconverged first and the non-.aligned form is used, so a caller
+// whose lane 0 just left a lane-0-only branch is still well defined.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------------------

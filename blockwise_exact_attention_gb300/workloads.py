@@ -66,16 +66,18 @@ WORKLOADS: dict[str, Workload] = {
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even); returns float32
-    arrays whose values are exactly representable in bf16."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    lsb = (bits >> 16) & 1
-    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
-    nan = np.isnan(x)
-    out = rounded.astype(np.uint32).view(np.float32).copy()
-    out[nan] = np.float32("nan")
-    return out.reshape(x.shape)
+    """Round finite float32 values to the nearest bf16 (ties to even); returns
+    float32 arrays whose values are exactly representable in bf16."""
+    x = np.array(x, dtype=np.float32, copy=True, order="C")
+    if not np.isfinite(x).all():
+        raise ValueError("round_to_bf16 expects finite inputs")
+    bits = x.view(np.uint32)
+    lsb = bits >> np.uint32(16)
+    lsb &= np.uint32(1)
+    lsb += np.uint32(0x7FFF)
+    bits += lsb            # |x| < 2^128 - 2^112, so this cannot carry into the sign bit
+    bits &= np.uint32(0xFFFF0000)
+    return x
 
 
 def rotary(x: np.ndarray, base: float = 10000.0) -> np.ndarray:

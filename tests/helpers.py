@@ -48,3 +48,14 @@ def to_dev(a: np.ndarray, dtype):
 def to_np(t) -> np.ndarray:
     import torch
     return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
+
+
+_INPUT_CACHE: dict = {}
+
+
+def cached_inputs(name: str) -> dict:
+    """make_inputs() of a named workload, generated once per test process."""
+    from blockwise_exact_attention_gb300 import workloads
+    if name not in _INPUT_CACHE:
+        _INPUT_CACHE[name] = workloads.make_inputs(workloads.WORKLOADS[name])
+    return _INPUT_CACHE[name]

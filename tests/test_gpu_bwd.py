@@ -16,7 +16,7 @@ import pytest
 import oracle
 from blockwise_exact_attention_gb300 import workloads
 
-from helpers import assert_close_bf16, to_dev, to_np
+from helpers import assert_close_bf16, cached_inputs, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -138,7 +138,7 @@ FULL = {
 def test_bwd_full_size_head_subset(name):
     import blockwise_exact_attention_gb300 as bea
     w = workloads.WORKLOADS[name]
-    x = workloads.make_inputs(w)
+    x = cached_inputs(name)
     g = w.h // w.h_kv
     kvs = FULL[name]
     hqs = [kv * g + t for kv in kvs for t in range(g)]

@@ -14,7 +14,7 @@ import pytest
 import oracle
 from blockwise_exact_attention_gb300 import workloads
 
-from helpers import TOL_LSE, assert_close, assert_close_bf16, to_dev, to_np
+from helpers import TOL_LSE, assert_close, assert_close_bf16, cached_inputs, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -122,7 +122,7 @@ FULL = ["causal_mha_4k", "causal_gqa_8k_rope", "swa_32k_d128", "full_32k_d64"]
 def test_fwd_full_size_sampled(name):
     import blockwise_exact_attention_gb300 as bea
     w = workloads.WORKLOADS[name]
-    x = workloads.make_inputs(w, with_dout=False)
+    x = cached_inputs(name)
     q, k, v = (to_dev(x[s], torch.bfloat16) for s in ("q", "k", "v"))
     out, lse = bea.flash_mha_fwd(q, k, v, w.softmax_scale, w.is_causal, w.window)
     torch.cuda.synchronize()

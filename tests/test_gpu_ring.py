@@ -10,7 +10,7 @@ import pytest
 import oracle
 from blockwise_exact_attention_gb300 import workloads
 
-from helpers import TOL_LSE, TOL_RING, assert_close, assert_close_bf16, to_dev, to_np
+from helpers import TOL_LSE, TOL_RING, assert_close, assert_close_bf16, cached_inputs, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -63,7 +63,7 @@ def test_ring_full_size():
     """[1, 16384, 16, 128] as 8 chunks of 2048: 36 chunk forwards, 28 merges."""
     import blockwise_exact_attention_gb300 as bea
     w = workloads.WORKLOADS["ring_causal_16k"]
-    x = workloads.make_inputs(w)
+    x = cached_inputs("ring_causal_16k")
     q, k, v, do = (to_dev(x[s], torch.bfloat16) for s in ("q", "k", "v", "dout"))
     s = w.softmax_scale
     bea.launches_since_reset(reset=True)
