@@ -34,7 +34,8 @@ def assert_close_bf16(got: np.ndarray, ref: np.ndarray, name: str, output_is_bf1
 def assert_close(got: np.ndarray, ref: np.ndarray, tol: float, name: str):
     got = got.astype(np.float64)
     both_inf = np.isneginf(got) & np.isneginf(ref)
-    err = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(got - ref))
     err = np.where(np.isnan(err), np.inf, err)
     assert err.max(initial=0.0) <= tol, f"{name}: max err {err.max():.3e} > {tol:.1e}"
     return float(err.max(initial=0.0))
