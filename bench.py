@@ -163,6 +163,29 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def run_only(which, fwd, bwd, dev, workloads, bea):
+    """A handful of launches of one kernel, nothing else timed (profiler runs)."""
+    import torch
+    if which == "fwd":
+        for _ in range(4):
+            fwd()
+    elif which == "bwd":
+        fwd()
+        for _ in range(4):
+            bwd()
+    else:
+        wr = workloads.WORKLOADS["ring_causal_16k"]
+        acc = torch.randn((1, wr.l, wr.h, wr.d), device=dev)
+        lacc = torch.randn((1, wr.h, wr.l), device=dev)
+        blk = torch.randn((1, wr.l, wr.h, wr.d), device=dev).to(torch.bfloat16)
+        lblk = torch.randn((1, wr.h, wr.l), device=dev)
+        for _ in range(4):
+            bea.ring_merge(acc, lacc, blk, lblk)
+    torch.cuda.synchronize()
+    print(json.dumps({"only": which, "status": bea.device_status()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -170,6 +193,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["fwd", "bwd", "merge"],
+                    help="run just this kernel a few times on the bench workload (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -227,6 +252,9 @@ def main():
             e1.synchronize()
             ts.append(e0.elapsed_time(e1))
         return ts
+
+    if args.only:
+        return run_only(args.only, fwd, bwd, dev, workloads, bea)
 
     # ---- headline: K steps of fwd + bwd, each step timed between L2 flushes ----
     for _ in range(args.warmup):
