@@ -40,6 +40,7 @@ EXPORTS = (
     "bea_version",
     "bea_selftest_wait_timeout",
     "bea_last_launch_count",
+    "bea_flash_mha_bwd_noalloc",
 )
 
 
@@ -91,6 +92,8 @@ def load() -> ctypes.CDLL:
     lib.bea_selftest_wait_timeout.restype = i
     lib.bea_last_launch_count.argtypes = []
     lib.bea_last_launch_count.restype = i
+    lib.bea_flash_mha_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, f, i, i, i, i, vp]
+    lib.bea_flash_mha_bwd_noalloc.restype = i
     _LIB = lib
     return lib
 

@@ -104,6 +104,21 @@ def flash_mha_bwd(dout, q, k, v, out, lse, softmax_scale=None, is_causal=False, 
     return dq, dk, dv
 
 
+def flash_mha_bwd_noalloc(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale=None, is_causal=False,
+                          window_size=(-1, -1), accumulate=False):
+    """flash_mha_bwd for callers that cannot allocate: the workspace is the
+    library's own fixed device array, and dq/dk/dv must be given."""
+    lib = _lib.load()
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[3])
+    ds = [_desc(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    rc = lib.bea_flash_mha_bwd_noalloc(*[_ref(x) for x in ds], float(softmax_scale), int(bool(is_causal)),
+                                       int(window_size[0]), int(window_size[1]), int(bool(accumulate)), _stream())
+    _lib.check(rc, "flash_mha_bwd_noalloc")
+    _count()
+    return dq, dk, dv
+
+
 def ring_merge(out_acc, lse_acc, out_blk, lse_blk, out_final=None):
     """Fold (out_blk, lse_blk) into the fp32 accumulator (out_acc, lse_acc) in place."""
     lib = _lib.load()

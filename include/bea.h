@@ -139,6 +139,37 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
                       void* stream);
 
 /*
+ * bea_flash_mha_bwd without a caller-supplied workspace. (The pages have no
+ * counterpart; this is a library convenience.)
+ *
+ * For callers that cannot allocate device memory: code that reaches the
+ * library only through a C function pointer from another language or plugin
+ * host that hands over just the tensors it owns, or a long-running serving
+ * loop that must not call cudaMalloc (which can synchronise the device). The
+ * workspace comes from a fixed array of BEA_NOALLOC_BWD_SCRATCH_BYTES in the
+ * library's own device memory; every GPU that loads the library holds that
+ * array until the process exits. This call allocates nothing.
+ *
+ * Arguments and results are those of bea_flash_mha_bwd. A problem whose
+ * workspace (bea_flash_mha_bwd_workspace_size) exceeds the array returns
+ * BEA_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture. All calls on a device share the one
+ * array, so two calls whose kernels may overlap on the GPU (different
+ * streams, or several host threads) race on it: order them on one stream.
+ * The array keeps the last call's contents; each call rewrites all of it
+ * that it reads, so nothing needs clearing between calls.
+ */
+#define BEA_NOALLOC_BWD_SCRATCH_BYTES (64u * 1024u * 1024u)
+int bea_flash_mha_bwd_noalloc(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k,
+                              const bea_tensor* v, const bea_tensor* out, const bea_tensor* lse,
+                              const bea_tensor* dq, const bea_tensor* dk, const bea_tensor* dv,
+                              float softmax_scale, int is_causal, int window_left, int window_right,
+                              int accumulate, void* stream);
+
+/*
  * Log-sum-exp merge, in place on the accumulator (flash_attn_jax
  * flash_sharding.py, "Ring Forward"; the same fold as picotron
  * update_out_and_lse in its sigmoid form). Per row r = (b, i, head):
