@@ -15,26 +15,24 @@
 //   2. main: one CTA per (128-key block, batch, K/V head). K and V stay in
 //      shared memory; the CTA walks the group's query heads x the 128-row
 //      query tiles the causal/window band lets it see:
-//        warp 8      TMA producer (K, V once; Q_i and dO_i into 2 stages),
-//        warp 9      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM,
-//                    then dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i and
-//                    dQ_i = dS K (dS^T from shared memory, read K-major for
-//                    dK and MN-major for dQ),
-//        warps 0-3   one thread per key: P^T and dS^T from S^T, dP^T, L2, D;
-//                    finally the dK/dV epilogue,
-//        warps 4-7   one thread per query row: move dQ_i out of TMEM and
-//                    bulk-reduce-add it (fp32) into the workspace.
+//        warp 8      producer: K, V once; per tile Q_i and dO_i (TMA) and the
+//                    tile's L2 and D rows (bulk copies) into 2 stages,
+//        warp 9      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM;
+//                    then, per 64-query half as soon as it is ready,
+//                    dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i and
+//                    dQ_i^T = K^T dS^T (dS^T from shared memory),
+//        warps 0-3   one thread per key: P^T and dS^T from S^T, dP^T, L2, D,
+//                    one 64-query half at a time; finally the dK/dV epilogue,
+//        warps 4-7   one thread per head-dim index: read dQ_i^T out of TMEM
+//                    and add it into the fp32 accumulator; the 32 lanes of a
+//                    warp cover 32 consecutive entries of a query row, so each
+//                    reduction instruction is one contiguous 128-byte line.
 //      dK and dV accumulate in TMEM across the whole group: no atomics.
 //   3. convert: dQ = scale * accumulator, cast or added into the caller's dq.
 //
 // TMEM (512 columns): S^T [0,128) (P^T packed bf16 over its first 64
-// columns), dP^T [128,256) (later dQ_i), dV [256,256+D), dK [384,384+D).
-//
-// Workspace dQ accumulator layout (fp32): per (b, head, 128-row query tile),
-// D/64 blocks of [128 rows x 64 columns]; inside a row, 16-byte chunk c is
-// stored at position c ^ (row & 15) so that the staging writes of a warp hit
-// distinct shared-memory banks. Every block is one contiguous 32 KB bulk
-// reduce.
+// columns), dP^T [128,256) (later dQ^T, 64 columns per query half),
+// dV [256,256+D), dK [384,384+D).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -48,7 +46,6 @@ constexpr int kBN = 128;  // keys per CTA
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr uint32_t kDrainBar = 1;  // named barrier of the drain warpgroup
 
 template <int D>
 struct BwdCfg {
@@ -58,20 +55,22 @@ struct BwdCfg {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;          // 2 stages
   static constexpr int kDOOff = kQOff + 2 * kTileBytes;     // 2 stages
-  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;    // dS^T [128 keys x 128 q] bf16, also dQ staging
+  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;    // dS^T [128 keys x 128 q] bf16
   static constexpr int kDSBytes = 128 * 128 * 2;
-  static constexpr int kBarOff = kDSOff + kDSBytes;
-  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 6 + 1;
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort, drain verdict*/ + 1024;
+  static constexpr int kRowOff = kDSOff + kDSBytes;         // 2 stages of L2[128], D[128] fp32
+  static constexpr int kBarOff = kRowOff + 2 * 1024;
+  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 1 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, false, true);     // dV (TMEM A), dK
-  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true, true);       // dQ
+  // dQ^T = K^T dS^T: M = 128 head-dim rows (for d = 64 the upper half are padding rows), N = 64 queries
+  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ float* dq_acc_tile(const BwdParams& p, int b, int hq, int qt) {
-  const int nqt = p.lq_pad / kBM;
-  return p.dq_acc + ((size_t)(b * p.a.h + hq) * nqt + qt) * (size_t)(kBM * p.a.d);
+// Row `i` of query head `hq` in the fp32 dQ accumulator ([n, h, lq_pad, d], row-major).
+__device__ __forceinline__ float* dq_acc_row(const BwdParams& p, int b, int hq, int i) {
+  return p.dq_acc + ((size_t)(b * p.a.h + hq) * p.lq_pad + i) * p.a.d;
 }
 
 // ---------------------------------------------------------------------------
@@ -120,13 +119,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdParams p) {
     p.d_row[row] = (i < a.lq) ? dsum : 0.f;
     p.lse2[row] = l2;
   }
-  // zero this row of the dQ accumulator (D/64 blocks of 64 floats, contiguous per block)
-  float* tile = dq_acc_tile(p, b, hq, i / kBM);
-  const int r = i % kBM;
-  for (int c = lane * 4; c < a.d; c += 128) {
-    const int blk = c / 64, cc = c % 64;
-    *reinterpret_cast<float4*>(tile + (size_t)blk * kBM * 64 + r * 64 + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  // zero this row of the dQ accumulator
+  float* acc = dq_acc_row(p, b, hq, i);
+  for (int c = lane * 4; c < a.d; c += 128) *reinterpret_cast<float4*>(acc + c) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -142,12 +137,9 @@ __global__ void __launch_bounds__(256) bwd_convert_dq_kernel(BwdParams p) {
   const int i = (int)(row % a.lq);
   const int bh = (int)(row / a.lq);
   const int hq = bh % a.h, b = bh / a.h;
-  const float* tile = dq_acc_tile(p, b, hq, i / kBM);
-  const int r = i % kBM;
+  const float* acc = dq_acc_row(p, b, hq, i);
   for (int c = lane * 4; c < a.d; c += 128) {
-    const int blk = c / 64, chunk = (c % 64) / 4;
-    const int phys = chunk ^ (r & 15);
-    float4 v = *reinterpret_cast<const float4*>(tile + (size_t)blk * kBM * 64 + r * 64 + phys * 4);
+    float4 v = *reinterpret_cast<const float4*>(acc + c);
     v.x *= a.scale;
     v.y *= a.scale;
     v.z *= a.scale;
@@ -191,28 +183,75 @@ __device__ __forceinline__ bool bwd_tile_needs_mask(const AttnDims& a, int k0, i
   return false;
 }
 
+// One 32-query chunk of the compute warpgroup: P^T and dS^T for this
+// thread's key row from S^T, dP^T (registers), L2 and D (shared memory).
+template <int D>
+__device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv, const float* l2s, const float* dds,
+                                          int cc, bool need_mask, const AttnDims& a, int kj, int q0, float scale_log2,
+                                          uint32_t s_t, uint8_t* ds_row, int j) {
+  uint32_t pk[16], dk[16];
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 L4 = *reinterpret_cast<const float4*>(l2s + cc * 32 + e4 * 4);
+    const float4 D4 = *reinterpret_cast<const float4*>(dds + cc * 32 + e4 * 4);
+    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+    const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+    float pr[4], dsr[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e4 * 4 + u;
+      float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, -Lv[u]));
+      if (need_mask) {
+        const int qi = q0 + cc * 32 + e;
+        if (!(kj < a.lk && key_visible(qi, kj, a.wl, a.wr))) pe = 0.f;
+      }
+      pr[u] = pe;
+      dsr[u] = pe * (__uint_as_float(pv[e]) - Dv[u]);
+    }
+    pk[e4 * 2] = pack_bf16x2(pr[0], pr[1]);
+    pk[e4 * 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+    dk[e4 * 2] = pack_bf16x2(dsr[0], dsr[1]);
+    dk[e4 * 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
+  }
+  // P^T (packed bf16 pairs) over S^T columns that this thread has already read
+  tmem_st16(s_t + cc * 16, pk);
+  // dS^T row j, queries [32cc, 32cc+32): 4 chunks of 16 B, 128-byte swizzle
+  uint8_t* half = ds_row + (cc >> 1) * 16384;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int chunk = (cc & 1) * 4 + u;
+    const int phys = chunk ^ (j & 7);
+    *reinterpret_cast<uint4*>(half + phys * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const BwdParams p, float scale_log2) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
+  uint64_t* q_full = bars + 1;        // Q_i, L2_i, D_i of a stage
   uint64_t* do_full = q_full + 2;
   uint64_t* qdo_empty = do_full + 2;
-  uint64_t* sp_full = qdo_empty + 2;
-  uint64_t* ds_ready = sp_full + 1;
-  uint64_t* dq_full = ds_ready + 1;
-  uint64_t* dq_empty = dq_full + 1;
-  uint64_t* ds_free = dq_empty + 1;
-  uint64_t* dkv_full = ds_free + 1;
+  uint64_t* sp_full = qdo_empty + 2;  // S^T and dP^T of an iteration are in TMEM
+  uint64_t* ready = sp_full + 1;      // [2]: P^T / dS^T of query half h written
+  uint64_t* dq_full = ready + 2;      // [2]: dQ^T of query half h in TMEM
+  uint64_t* dq_empty = dq_full + 2;   // [2]: dQ^T of query half h read out
+  uint64_t* dkv_full = dq_empty + 2;
   uint64_t* mma_done = dkv_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  // The swizzled operand tiles need 1024-byte alignment; the dynamic shared
+  // window starts there when the kernel has no static shared memory.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) report_status(p.status, BEA_STATUS_CONFIG);
+    return;
+  }
 
   const AttnDims& a = p.a;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -246,12 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&do_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
+      mbar_init(&ready[s], 128);
+      mbar_init(&dq_full[s], 1);
+      mbar_init(&dq_empty[s], 128);
     }
     mbar_init(sp_full, 1);
-    mbar_init(ds_ready, 128);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
-    mbar_init(ds_free, 1);
     mbar_init(dkv_full, 1);
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -284,9 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hq = kvh * sc.g + it / nt;
         const int q0 = (sc.i_lo + it % nt) * kBM;
         if (it >= 2 && !wait_parity(&qdo_empty[s], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
+        mbar_arrive_expect_tx(&q_full[s], C::kTileBytes + 2 * kBM * 4);
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d(smem + C::kQOff + s * C::kTileBytes + x * 16384, &tq, &q_full[s], x * 64, hq, q0, b);
+        const size_t row0 = (size_t)(b * a.h + hq) * p.lq_pad + q0;
+        bulk_load(smem + C::kRowOff + s * 1024, p.lse2 + row0, kBM * 4, &q_full[s]);
+        bulk_load(smem + C::kRowOff + s * 1024 + 512, p.d_row + row0, kBM * 4, &q_full[s]);
         mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d(smem + C::kDOOff + s * C::kTileBytes + x * 16384, &tdo, &do_full[s], x * 64, hq, q0, b);
@@ -313,14 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t do_addr = smem_u32(smem + C::kDOOff + s * C::kTileBytes);
         if (!(ok = wait_parity(&q_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
-        // S^T = K Q^T   (M = keys, N = queries, K = d; both K-major)
+        // S^T = K Q^T   (M = keys, N = 128 queries, K = d; both K-major)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
           umma_ss(tmem + T_S, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024), C::kIdescS,
                   k > 0 ? 1u : 0u);
         }
-        if (it > 0 && !(ok = wait_parity(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
+        if (it > 0) {
+          // dQ^T of the previous iteration occupies the dP^T columns until read out
+          if (!(ok = wait_parity(&dq_empty[0], (it - 1) & 1, abort_flag, p.status))) break;
+          if (!(ok = wait_parity(&dq_empty[1], (it - 1) & 1, abort_flag, p.status))) break;
+        }
         if (!(ok = wait_parity(&do_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
         // dP^T = V dO^T
@@ -331,26 +376,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                   C::kIdescS, k > 0 ? 1u : 0u);
         }
         umma_commit(sp_full);
-        if (!(ok = wait_parity(ds_ready, it & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // dV += P^T dO    (A = P^T from TMEM, B = dO MN-major)
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = wait_parity(&ready[h], it & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          // dV += P^T dO over queries [64h, 64h+64)   (A = P^T from TMEM, B = dO MN-major)
 #pragma unroll
-        for (int k = 0; k < kBM / 16; ++k)
-          umma_ts(tmem + T_DV, tmem + T_S + k * 8, sdesc_sw128(do_addr + k * 2048, 16384, 1024), C::kIdescKV,
-                  (it > 0 || k > 0) ? 1u : 0u);
-        // dK += dS^T Q    (A = dS^T K-major, B = Q MN-major)
+          for (int k = 0; k < 4; ++k)
+            umma_ts(tmem + T_DV, tmem + T_S + (4 * h + k) * 8, sdesc_sw128(do_addr + (4 * h + k) * 2048, 16384, 1024),
+                    C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+          // dK += dS^T Q over the same queries        (A = dS^T K-major, B = Q MN-major)
 #pragma unroll
-        for (int k = 0; k < kBM / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + T_DK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(q_addr + k * 2048, 16384, 1024),
-                  C::kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_DK, sdesc_sw128(ds_addr + h * 16384 + k * 32, 16, 1024),
+                    sdesc_sw128(q_addr + (4 * h + k) * 2048, 16384, 1024), C::kIdescKV,
+                    (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+          // dQ^T[:, half] = K^T dS^T[:, half]       (A = K read MN-major, B = dS^T MN-major), into dP^T columns
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            umma_ss(tmem + T_DP + 64 * h, sdesc_sw128(k_addr + k * 2048, 16384, 1024),
+                    sdesc_sw128(ds_addr + h * 16384 + k * 2048, 16384, 1024), C::kIdescQ, k > 0 ? 1u : 0u);
+          umma_commit(&dq_full[h]);
         }
-        // dQ = dS K       (A = dS^T buffer read MN-major, B = K MN-major), into the dP^T columns
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          umma_ss(tmem + T_DP, sdesc_sw128(ds_addr + k * 2048, 16384, 1024), sdesc_sw128(k_addr + k * 2048, 16384, 1024),
-                  C::kIdescQ, k > 0 ? 1u : 0u);
-        umma_commit(dq_full);
+        if (!ok) break;
         umma_commit(&qdo_empty[s]);
       }
       if (ok && sc.n_iter > 0) umma_commit(dkv_full);
@@ -368,61 +415,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_row = smem + C::kDSOff + j * 128;
     bool ok = true;
     for (int it = 0; it < sc.n_iter; ++it) {
-      const int hq = kvh * sc.g + it / nt;
+      const int s = it & 1;
       const int q0 = (sc.i_lo + it % nt) * kBM;
+      // S^T, dP^T of this iteration; it also means every MMA of the previous
+      // iteration (the readers of the dS^T buffer and of P^T) has completed
       if (!(ok = warp_wait_parity(sp_full, it & 1, abort_flag, p.status))) break;
-      if (it > 0 && !(ok = warp_wait_parity(ds_free, (it - 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
       const bool need_mask = bwd_tile_needs_mask(a, sc.k0, q0);
-      const float* l2 = p.lse2 + (size_t)(b * a.h + hq) * p.lq_pad + q0;
-      const float* dd = p.d_row + (size_t)(b * a.h + hq) * p.lq_pad + q0;
+      const float* l2s = reinterpret_cast<const float*>(smem + C::kRowOff + s * 1024);
+      const float* dds = l2s + kBM;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(s_t + cc * 32, sv);
-        tmem_ld32(dp_t + cc * 32, pv);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sv0[32], pv0[32], sv1[32], pv1[32];
+        tmem_ld32(s_t + 64 * h, sv0);
+        tmem_ld32(dp_t + 64 * h, pv0);
         tmem_wait_ld();
-        reg_fence<32>(sv);
-        reg_fence<32>(pv);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 L4 = *reinterpret_cast<const float4*>(l2 + cc * 32 + e4 * 4);
-          const float4 D4 = *reinterpret_cast<const float4*>(dd + cc * 32 + e4 * 4);
-          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
-          const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-          float pr[4], dsr[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = e4 * 4 + u;
-            float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, -Lv[u]));
-            if (need_mask) {
-              const int qi = q0 + cc * 32 + e;
-              if (!(kj < a.lk && key_visible(qi, kj, a.wl, a.wr))) pe = 0.f;
-            }
-            pr[u] = pe;
-            dsr[u] = pe * (__uint_as_float(pv[e]) - Dv[u]);
-          }
-          pk[e4 * 2] = pack_bf16x2(pr[0], pr[1]);
-          pk[e4 * 2 + 1] = pack_bf16x2(pr[2], pr[3]);
-          dk[e4 * 2] = pack_bf16x2(dsr[0], dsr[1]);
-          dk[e4 * 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
-        }
-        // P^T (packed bf16 pairs) over the S^T columns already read
-        tmem_st16(s_t + cc * 16, pk);
-        // dS^T row j, queries [32cc, 32cc+32): 4 chunks of 16 B, 128-byte swizzle
-        uint8_t* half = ds_row + (cc >> 1) * 16384;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = (cc & 1) * 4 + u;
-          const int phys = chunk ^ (j & 7);
-          *reinterpret_cast<uint4*>(half + phys * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
+        reg_fence<32>(sv0);
+        reg_fence<32>(pv0);
+        tmem_ld32(s_t + 64 * h + 32, sv1);  // in flight while chunk 2h is processed
+        tmem_ld32(dp_t + 64 * h + 32, pv1);
+        bwd_chunk<D>(sv0, pv0, l2s, dds, 2 * h, need_mask, a, kj, q0, scale_log2, s_t, ds_row, j);
+        tmem_wait_ld();
+        reg_fence<32>(sv1);
+        reg_fence<32>(pv1);
+        bwd_chunk<D>(sv1, pv1, l2s, dds, 2 * h + 1, need_mask, a, kj, q0, scale_log2, s_t, ds_row, j);
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(&ready[h]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(ds_ready);
     }
     // ---- dK / dV epilogue ----
     if (ok && sc.n_iter > 0) ok = warp_wait_parity(dkv_full, 0, abort_flag, p.status);
@@ -444,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < 32; ++c) kk[c] = __float_as_uint(__uint_as_float(kk[c]) * a.scale);
-        if (kj >= a.lk) continue;  // ragged last key block: loads above stay warp-wide
+        if (kj >= a.lk) continue;  // ragged last key block: the loads above stay warp-wide
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t* src = which ? kk : vv;
@@ -483,48 +504,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    // ========================== dQ drain (one thread per query row) ==========================
-    const int r = threadIdx.x - 128;  // query row within the tile == TMEM lane
+    // ========================== dQ drain (one thread per head-dim index) ==========================
+    const int dd = threadIdx.x - 128;  // dQ^T row == head-dim index == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
     const uint32_t dq_t = tmem + lane_base + T_DP;
-    uint8_t* stage = smem + C::kDSOff;
-    volatile int* drain_ok = abort_flag + 1;  // one thread waits, the group follows its verdict
+    const bool live = dd < D;  // for d = 64 the upper 64 lanes hold padding rows
     for (int it = 0; it < sc.n_iter; ++it) {
       const int hq = kvh * sc.g + it / nt;
-      const int qt = sc.i_lo + it % nt;
-      if (r == 0) *drain_ok = wait_parity(dq_full, it & 1, abort_flag, p.status) ? 1 : 0;
-      named_bar_sync(kDrainBar, 128);
-      if (!*drain_ok) break;
-      tc_fence_after();
-      uint32_t v[D];
+      const int q0 = (sc.i_lo + it % nt) * kBM;
+      float* dst = p.dq_acc + ((size_t)(b * a.h + hq) * p.lq_pad + q0) * D + dd;
+      bool ok = true;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = warp_wait_parity(&dq_full[h], it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld32(dq_t + 64 * h, v);
+        tmem_ld32(dq_t + 64 * h + 32, v + 32);
+        tmem_wait_ld();
+        reg_fence<64>(v);
+        tc_fence_before();
+        mbar_arrive(&dq_empty[h]);
+        if (live) {
+          // lanes of a warp hold 32 consecutive head-dim entries of one query row:
+          // each reduction instruction covers one contiguous 128-byte line
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(dq_t + c0, v + c0);
-      tmem_wait_ld();
-      reg_fence<D>(v);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      float* dst = dq_acc_tile(p, b, hq, qt);
-#pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk) {
-        // the dS^T buffer is free: dK and dQ of this iteration have completed
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int phys = c ^ (r & 15);
-          *reinterpret_cast<uint4*>(stage + r * 256 + phys * 16) =
-              make_uint4(v[blk * 64 + 4 * c], v[blk * 64 + 4 * c + 1], v[blk * 64 + 4 * c + 2], v[blk * 64 + 4 * c + 3]);
+          for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)(64 * h + c) * D, __uint_as_float(v[c]));
         }
-        fence_proxy_async_smem();
-        named_bar_sync(kDrainBar, 128);
-        if (r == 0) {
-          bulk_reduce_add_f32(dst + (size_t)blk * kBM * 64, stage, kBM * 64 * 4);
-          bulk_commit_group();
-          bulk_wait_group_read<0>();
-        }
-        named_bar_sync(kDrainBar, 128);
       }
-      if (r == 0) mbar_arrive(ds_free);
+      if (!ok) break;
     }
-    if (r == 0) bulk_wait_group<0>();
   }
 
   // ---- teardown ----
