@@ -43,7 +43,16 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per iteration
 constexpr int kBN = 128;  // keys per CTA
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;  // 3 warpgroups
+// Register split: launched at kRegsLaunch per thread (65536 / 384 rounded
+// down to 8); the key-row warpgroup rises to kRegsCompute, the dQ drain and
+// the producer/MMA warpgroup drop to kRegsDrain and kRegsOther:
+// 128 * (224 + 160 + 120) = 384 * 168.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsCompute = 224;
+constexpr int kRegsDrain = 160;
+constexpr int kRegsOther = 120;
+static_assert(kRegsCompute + kRegsDrain + kRegsOther == 3 * kRegsLaunch, "register split");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 
@@ -304,6 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384;
 
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
   if (warp == kProducerWarp) {
     // ========================== TMA producer ==========================
     if (lane == 0 && sc.n_iter > 0) {
@@ -343,23 +354,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ========================== MMA issuer ==========================
     if (lane == 0) {
-      const uint32_t k_addr = smem_u32(smem + C::kKOff);
-      const uint32_t v_addr = smem_u32(smem + C::kVOff);
-      const uint32_t ds_addr = smem_u32(smem + C::kDSOff);
+      // base descriptors (K-major: LBO unused; MN-major: 64-element blocks 16 KB apart)
+      const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(smem + C::kKOff), 16384, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + C::kVOff), 16, 1024);
+      const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + C::kDSOff), 16, 1024);
+      const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + C::kDSOff), 16384, 1024);
+      const uint64_t q_kmaj0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+      const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16384, 1024);
+      const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + C::kDOOff), 16, 1024);
+      const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + C::kDOOff), 16384, 1024);
       bool ok = sc.n_iter > 0 && wait_parity(kv_full, 0, abort_flag, p.status);
       for (int it = 0; ok && it < sc.n_iter; ++it) {
         const int s = it & 1;
         const uint32_t par = (it >> 1) & 1;
-        const uint32_t q_addr = smem_u32(smem + C::kQOff + s * C::kTileBytes);
-        const uint32_t do_addr = smem_u32(smem + C::kDOOff + s * C::kTileBytes);
+        const uint64_t q_kmaj = sdesc_add(q_kmaj0, s * C::kTileBytes);
+        const uint64_t q_mn = sdesc_add(q_mn0, s * C::kTileBytes);
+        const uint64_t do_kmaj = sdesc_add(do_kmaj0, s * C::kTileBytes);
+        const uint64_t do_mn = sdesc_add(do_mn0, s * C::kTileBytes);
         if (!(ok = wait_parity(&q_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
         // S^T = K Q^T   (M = keys, N = 128 queries, K = d; both K-major)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + T_S, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024), C::kIdescS,
-                  k > 0 ? 1u : 0u);
+          umma_ss(tmem + T_S, sdesc_add(k_kmaj, off), sdesc_add(q_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
         }
         if (it > 0) {
           // dQ^T of the previous iteration occupies the dP^T columns until read out
@@ -372,8 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + T_DP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
-                  C::kIdescS, k > 0 ? 1u : 0u);
+          umma_ss(tmem + T_DP, sdesc_add(v_kmaj, off), sdesc_add(do_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
         }
         umma_commit(sp_full);
         for (int h = 0; h < 2; ++h) {
@@ -382,19 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dV += P^T dO over queries [64h, 64h+64)   (A = P^T from TMEM, B = dO MN-major)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_ts(tmem + T_DV, tmem + T_S + (4 * h + k) * 8, sdesc_sw128(do_addr + (4 * h + k) * 2048, 16384, 1024),
-                    C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+            umma_ts(tmem + T_DV, tmem + T_S + (4 * h + k) * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
+                    (it > 0 || h > 0 || k > 0) ? 1u : 0u);
           // dK += dS^T Q over the same queries        (A = dS^T K-major, B = Q MN-major)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_DK, sdesc_sw128(ds_addr + h * 16384 + k * 32, 16, 1024),
-                    sdesc_sw128(q_addr + (4 * h + k) * 2048, 16384, 1024), C::kIdescKV,
-                    (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+            umma_ss(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
+                    C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
           // dQ^T[:, half] = K^T dS^T[:, half]       (A = K read MN-major, B = dS^T MN-major), into dP^T columns
 #pragma unroll
           for (int k = 0; k < kBN / 16; ++k)
-            umma_ss(tmem + T_DP + 64 * h, sdesc_sw128(k_addr + k * 2048, 16384, 1024),
-                    sdesc_sw128(ds_addr + h * 16384 + k * 2048, 16384, 1024), C::kIdescQ, k > 0 ? 1u : 0u);
+            umma_ss(tmem + T_DP + 64 * h, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048), C::kIdescQ,
+                    k > 0 ? 1u : 0u);
           umma_commit(&dq_full[h]);
         }
         if (!ok) break;
@@ -405,7 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       wait_parity(mma_done, 0, &no_abort, p.status, 200000000ull);
     }
+  }
   } else if (warp < 4) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
     // ========================== P^T / dS^T (one thread per key) ==========================
     const int j = threadIdx.x;  // key row == TMEM lane
     const int kj = sc.k0 + j;
@@ -503,7 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < 8) {
+  } else {
+    static_assert(kRegsDrain <= kRegsLaunch, "the drain warpgroup gives registers back");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDrain));
     // ========================== dQ drain (one thread per head-dim index) ==========================
     const int dd = threadIdx.x - 128;  // dQ^T row == head-dim index == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
@@ -565,6 +586,12 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
   if (blocks > 0) {
     e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // The register split is only sound at exactly kRegsLaunch registers per
+    // thread; refuse to launch otherwise (setmaxnreg.inc would never return).
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     const float scale_log2 = a.scale * 1.4426950408889634f;
     bwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p, scale_log2);
     *nlaunch += 1;

@@ -222,24 +222,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_addr = smem_u32(smem + C::kVOff);
       int pv_count[kSub] = {0, 0};
       bool ok = true;
+      // base descriptors; every operand below is an offset from one of them
+      const uint64_t q_desc = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(k_addr, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(v_addr, C::kVLbo, 1024);
       auto issue_s = [&](int t, int s) {
-        const uint32_t qa = q_addr + t * C::kTileBytes;
-        const uint32_t ka = k_addr + s * C::kTileBytes;
+        const uint64_t qd = sdesc_add(q_desc, t * C::kTileBytes);
+        const uint64_t kd = sdesc_add(k_desc, s * C::kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), C::kIdescS,
-                  k > 0 ? 1u : 0u);
+          umma_ss(tmem + t * 128, sdesc_add(qd, off), sdesc_add(kd, off), C::kIdescS, k > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int s) {
-        const uint32_t va = v_addr + s * C::kTileBytes;
+        const uint64_t vd = sdesc_add(v_desc, s * C::kTileBytes);
+        const uint32_t acc0 = pv_count[t] > 0 ? 1u : 0u;
 #pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k) {
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_sw128(va + k * 2048, C::kVLbo, 1024),
-                  C::kIdescPV, (pv_count[t] > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kBlockN / 16; ++k)
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_add(vd, k * 2048), C::kIdescPV, k > 0 ? 1u : acc0);
         ++pv_count[t];
       };
       auto active = [&](int t, int j) { return j >= sc.lo[t] && j < sc.hi[t]; };
@@ -330,10 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(kj < a.lk && key_visible(qi, kj, a.wl, a.wr))) sr[c] = __float_as_uint(-INFINITY);
         }
       }
-      // softmax_scale > 0, so the max commutes with the scaling
-      float mx = __uint_as_float(sr[0]);
+      // softmax_scale > 0, so the max commutes with the scaling. Eight
+      // independent partial maxima keep the dependent chain short.
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(sr[c]);
+#pragma unroll
+      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       mx *= scale_log2;
       const float m_new = fmaxf(m_ref, mx);
       const bool grow = m_new > m_ref + kRescaleThreshold;  // also true when m_ref = -inf, m_new finite
@@ -351,15 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       uint32_t pk[64];
-      float psum = 0.f;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, neg_m));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, neg_m));
-        psum += p0 + p1;
+        ps[c & 7] += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      l_sum += psum;
+      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       tmem_st32(s_tmem + 0, pk);
       tmem_st32(s_tmem + 32, pk + 32);
       if (rescale) {

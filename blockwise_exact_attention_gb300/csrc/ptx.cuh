@@ -276,6 +276,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of the same operand `bytes` further on: the start address sits
+// in the low 14 bits in 16-byte units and never carries out of them (shared
+// memory is < 256 KB), so advancing is one 64-bit add.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // D[tmem] (+)= A[smem] * B[smem], operands as described. One thread issues.
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
