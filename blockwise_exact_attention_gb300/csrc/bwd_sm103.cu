@@ -194,9 +194,11 @@ __device__ __forceinline__ bool bwd_tile_needs_mask(const AttnDims& a, int k0, i
 
 // One 32-query chunk of the compute warpgroup: P^T and dS^T for this
 // thread's key row from S^T, dP^T (registers), L2 and D (shared memory).
-template <int D>
+// The mask decision is a template parameter so that the unrolled element
+// loop has no branches and the 32 independent element chains interleave.
+template <int D, bool kMask>
 __device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv, const float* l2s, const float* dds,
-                                          int cc, bool need_mask, const AttnDims& a, int kj, int q0, float scale_log2,
+                                          int cc, const AttnDims& a, int kj, int q0, float scale_log2,
                                           uint32_t s_t, uint8_t* ds_row, int j) {
   uint32_t pk[16], dk[16];
 #pragma unroll
@@ -210,9 +212,10 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv
     for (int u = 0; u < 4; ++u) {
       const int e = e4 * 4 + u;
       float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, -Lv[u]));
-      if (need_mask) {
+      if constexpr (kMask) {
         const int qi = q0 + cc * 32 + e;
-        if (!(kj < a.lk && key_visible(qi, kj, a.wl, a.wr))) pe = 0.f;
+        const bool vis = (kj < a.lk) & key_visible(qi, kj, a.wl, a.wr);
+        pe = vis ? pe : 0.f;
       }
       pr[u] = pe;
       dsr[u] = pe * (__uint_as_float(pv[e]) - Dv[u]);
@@ -453,11 +456,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<32>(pv0);
         tmem_ld32(s_t + 64 * h + 32, sv1);  // in flight while chunk 2h is processed
         tmem_ld32(dp_t + 64 * h + 32, pv1);
-        bwd_chunk<D>(sv0, pv0, l2s, dds, 2 * h, need_mask, a, kj, q0, scale_log2, s_t, ds_row, j);
+        if (need_mask)
+          bwd_chunk<D, true>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, s_t, ds_row, j);
+        else
+          bwd_chunk<D, false>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, s_t, ds_row, j);
         tmem_wait_ld();
         reg_fence<32>(sv1);
         reg_fence<32>(pv1);
-        bwd_chunk<D>(sv1, pv1, l2s, dds, 2 * h + 1, need_mask, a, kj, q0, scale_log2, s_t, ds_row, j);
+        if (need_mask)
+          bwd_chunk<D, true>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, s_t, ds_row, j);
+        else
+          bwd_chunk<D, false>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, s_t, ds_row, j);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
