@@ -42,10 +42,10 @@ constexpr int kThreads = 384;  // 3 warpgroups
 // Register split: launched at kRegsLaunch per thread (65536 / 384 rounded
 // down to 8); the softmax warpgroups raise to kRegsSoftmax and the
 // producer/MMA warpgroup lowers to kRegsOther, which sums to the launch:
-// 256 * 216 + 128 * 72 = 384 * 168.
+// 256 * 208 + 128 * 88 = 384 * 168.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsSoftmax = 216;
-constexpr int kRegsOther = 72;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch, "register split");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -217,83 +217,84 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ========================== MMA issuer ==========================
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(smem + C::kQOff);
-      const uint32_t k_addr = smem_u32(smem + C::kKOff);
-      const uint32_t v_addr = smem_u32(smem + C::kVOff);
-      int pv_count[kSub] = {0, 0};
-      bool ok = true;
       // base descriptors; every operand below is an offset from one of them
-      const uint64_t q_desc = sdesc_sw128(q_addr, 16, 1024);
-      const uint64_t k_desc = sdesc_sw128(k_addr, 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(v_addr, C::kVLbo, 1024);
-      auto issue_s = [&](int t, int s) {
-        const uint64_t qd = sdesc_add(q_desc, t * C::kTileBytes);
-        const uint64_t kd = sdesc_add(k_desc, s * C::kTileBytes);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + t * 128, sdesc_add(qd, off), sdesc_add(kd, off), C::kIdescS, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[t]);
-      };
-      auto issue_pv = [&](int t, int s) {
-        const uint64_t vd = sdesc_add(v_desc, s * C::kTileBytes);
-        const uint32_t acc0 = pv_count[t] > 0 ? 1u : 0u;
-#pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_add(vd, k * 2048), C::kIdescPV, k > 0 ? 1u : acc0);
-        ++pv_count[t];
-      };
-      auto active = [&](int t, int j) { return j >= sc.lo[t] && j < sc.hi[t]; };
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::kVOff), C::kVLbo, 1024);
+      const int lo0 = sc.lo[0], hi0 = sc.hi[0], lo1 = sc.lo[1], hi1 = sc.hi[1];
+      const int lo_all = sc.lo_all, hi_all = sc.hi_all;
+      int pv0 = 0, pv1 = 0;  // P V products issued per subtile
+      bool ok = true;
+// S_t = Q_t K^T from K stage `stg` (one 16-wide K step per MMA)
+#define BEA_ISSUE_S(t, stg)                                                                          \
+  do {                                                                                               \
+    const uint64_t qd_ = sdesc_add(q_desc, (t) * C::kTileBytes);                                     \
+    const uint64_t kd_ = sdesc_add(k_desc, (stg) * C::kTileBytes);                                   \
+    _Pragma("unroll") for (int k_ = 0; k_ < D / 16; ++k_) {                                          \
+      const uint32_t off_ = (k_ / 4) * 16384 + (k_ % 4) * 32;                                        \
+      umma_ss(tmem + (t) * 128, sdesc_add(qd_, off_), sdesc_add(kd_, off_), C::kIdescS, k_ > 0 ? 1u : 0u); \
+    }                                                                                                \
+    umma_commit(&s_full[t]);                                                                         \
+  } while (0)
+// O_t (+)= P_t V from V stage `stg`; P_t is read from TMEM over S_t
+#define BEA_ISSUE_PV(t, stg, first)                                                                  \
+  do {                                                                                               \
+    const uint64_t vd_ = sdesc_add(v_desc, (stg) * C::kTileBytes);                                   \
+    _Pragma("unroll") for (int k_ = 0; k_ < kBlockN / 16; ++k_)                                      \
+      umma_ts(tmem + 256 + (t) * 128, tmem + (t) * 128 + k_ * 8, sdesc_add(vd_, k_ * 2048), C::kIdescPV, \
+              (k_ > 0 || !(first)) ? 1u : 0u);                                                       \
+  } while (0)
 
-      if (sc.hi_all > sc.lo_all) {
+      if (hi_all > lo_all) {
         ok = wait_parity(q_full, 0, abort_flag, p.status);
         if (ok) ok = wait_parity(&k_full[0], 0, abort_flag, p.status);
         if (ok) {
           tc_fence_after();
-          for (int t = 0; t < kSub; ++t)
-            if (active(t, sc.lo_all)) issue_s(t, 0);
+          if (lo0 == lo_all && hi0 > lo0) BEA_ISSUE_S(0, 0);
+          if (lo1 == lo_all && hi1 > lo1) BEA_ISSUE_S(1, 0);
         }
         int it = 0;
-        for (int j = sc.lo_all; ok && j < sc.hi_all; ++j, ++it) {
+        for (int j = lo_all; ok && j < hi_all; ++j, ++it) {
           const int s = it % C::kStages;
           const uint32_t par = (it / C::kStages) & 1;
           const int s1 = (it + 1) % C::kStages;
           const uint32_t par1 = ((it + 1) / C::kStages) & 1;
+          const bool a0 = j >= lo0 && j < hi0, a1 = j >= lo1 && j < hi1;
+          const bool n0 = j + 1 >= lo0 && j + 1 < hi0, n1 = j + 1 >= lo1 && j + 1 < hi1;
           bool k_next_ready = false;
           if (!(ok = wait_parity(&v_full[s], par, abort_flag, p.status))) break;
-          for (int t = 0; t < kSub && ok; ++t) {
-            if (!active(t, j)) continue;
-            if (!(ok = wait_parity(&p_full[t], pv_count[t] & 1, abort_flag, p.status))) break;
+          if (a0) {
+            if (!(ok = wait_parity(&p_full[0], pv0 & 1, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_pv(t, s);
-            if (j + 1 < sc.hi_all && active(t, j + 1)) {
-              if (!k_next_ready) {
-                if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
-                tc_fence_after();
-                k_next_ready = true;
-              }
-              issue_s(t, s1);
-            }
+            BEA_ISSUE_PV(0, s, pv0 == 0);
+            ++pv0;
           }
-          if (!ok) break;
-          // a subtile whose band starts at tile j+1 still needs its first S
-          for (int t = 0; t < kSub && ok; ++t) {
-            if (j + 1 < sc.hi_all && !active(t, j) && active(t, j + 1)) {
-              if (!k_next_ready) {
-                if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
-                tc_fence_after();
-                k_next_ready = true;
-              }
-              issue_s(t, s1);
-            }
+          if (n0) {
+            if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
+            tc_fence_after();
+            k_next_ready = true;
+            BEA_ISSUE_S(0, s1);
           }
-          if (!ok) break;
+          if (a1) {
+            if (!(ok = wait_parity(&p_full[1], pv1 & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            BEA_ISSUE_PV(1, s, pv1 == 0);
+            ++pv1;
+          }
+          if (n1) {
+            if (!k_next_ready) {
+              if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
+              tc_fence_after();
+            }
+            BEA_ISSUE_S(1, s1);
+          }
           umma_commit(&kv_empty[s]);
-          for (int t = 0; t < kSub; ++t)
-            if (j == sc.hi[t] - 1) umma_commit(&o_full[t]);
+          if (j == hi0 - 1) umma_commit(&o_full[0]);
+          if (j == hi1 - 1) umma_commit(&o_full[1]);
         }
       }
+#undef BEA_ISSUE_S
+#undef BEA_ISSUE_PV
       // Everything issued must finish before TMEM is released.
       umma_commit(mma_done);
       volatile int no_abort = 0;
@@ -314,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_sum = 0.f;
     bool ok = true;
     int it = 0;
-    for (int j = sc.lo[t]; j < sc.hi[t]; ++j, ++it) {
+    const int my_lo = t ? sc.lo[1] : sc.lo[0], my_hi = t ? sc.hi[1] : sc.hi[0];  // no dynamic indexing
+    for (int j = my_lo; j < my_hi; ++j, ++it) {
       if (!(ok = warp_wait_parity(&s_full[t], it & 1, abort_flag, p.status))) break;
       tc_fence_after();
       uint32_t sr[128];
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[t]);
     }
     // ---- epilogue ----
-    const bool have_o = sc.lo[t] < sc.hi[t];
+    const bool have_o = my_lo < my_hi;
     if (ok && have_o) ok = warp_wait_parity(&o_full[t], 0, abort_flag, p.status);
     if (ok && qs < a.lq) {
       tc_fence_after();

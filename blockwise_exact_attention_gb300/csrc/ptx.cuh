@@ -284,14 +284,17 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
 }
 
 // D[tmem] (+)= A[smem] * B[smem], operands as described. One thread issues.
+// No "memory" clobber: the MMA reads shared memory asynchronously, ordered by
+// the mbarrier waits (which do clobber memory) and by the program order of
+// volatile asm; a clobber here would only force needless reloads between
+// consecutive MMAs of the issuing thread.
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]. A is M rows (lanes) x K packed bf16 pairs
@@ -302,8 +305,7 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive once on `bar` when all previously issued tcgen05 MMAs of this
