@@ -68,12 +68,12 @@ struct BwdCfg {
   static constexpr int kDSBytes = 128 * 128 * 2;
   static constexpr int kRowOff = kDSOff + kDSBytes;         // 2 stages of L2[128], D[128] fp32
   static constexpr int kBarOff = kRowOff + 2 * 1024;
-  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 1 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 1 + 2 + 1 + 1 + 1 + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, false, true);     // dV (TMEM A), dK
-  // dQ^T = K^T dS^T: M = 128 head-dim rows (for d = 64 the upper half are padding rows), N = 64 queries
-  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
+  // dQ^T = K^T dS^T: M = 128 head-dim rows (for d = 64 the upper half are padding rows), N = 128 queries
+  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 128, true, true);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qdo_empty = do_full + 2;
   uint64_t* sp_full = qdo_empty + 2;  // S^T and dP^T of an iteration are in TMEM
   uint64_t* ready = sp_full + 1;      // [2]: P^T / dS^T of query half h written
-  uint64_t* dq_full = ready + 2;      // [2]: dQ^T of query half h in TMEM
-  uint64_t* dq_empty = dq_full + 2;   // [2]: dQ^T of query half h read out
-  uint64_t* dkv_full = dq_empty + 2;
+  uint64_t* dq_full = ready + 2;      // dQ^T of the tile in TMEM
+  uint64_t* dq_empty = dq_full + 1;   // dQ^T of the tile read out
+  uint64_t* dkv_full = dq_empty + 1;
   uint64_t* mma_done = dkv_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -298,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&do_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
       mbar_init(&ready[s], 128);
-      mbar_init(&dq_full[s], 1);
-      mbar_init(&dq_empty[s], 128);
     }
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
     mbar_init(sp_full, 1);
     mbar_init(dkv_full, 1);
     mbar_init(mma_done, 1);
@@ -385,8 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (it > 0) {
           // dQ^T of the previous iteration occupies the dP^T columns until read out
-          if (!(ok = wait_parity(&dq_empty[0], (it - 1) & 1, abort_flag, p.status))) break;
-          if (!(ok = wait_parity(&dq_empty[1], (it - 1) & 1, abort_flag, p.status))) break;
+          if (!(ok = wait_parity(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
         }
         if (!(ok = wait_parity(&do_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
@@ -410,14 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k)
             umma_ss(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
                     C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
-          // dQ^T[:, half] = K^T dS^T[:, half]       (A = K read MN-major, B = dS^T MN-major), into dP^T columns
-#pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            umma_ss(tmem + T_DP + 64 * h, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048), C::kIdescQ,
-                    k > 0 ? 1u : 0u);
-          umma_commit(&dq_full[h]);
         }
         if (!ok) break;
+        // dQ^T = K^T dS^T over all 128 queries in one N = 128 product (A = K read
+        // MN-major, B = dS^T MN-major), into the dP^T columns
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          umma_ss(tmem + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, k * 2048), C::kIdescQ, k > 0 ? 1u : 0u);
+        umma_commit(dq_full);
         umma_commit(&qdo_empty[s]);
       }
       if (ok && sc.n_iter > 0) umma_commit(dkv_full);
@@ -543,26 +542,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int hq = kvh * sc.g + it / nt;
       const int q0 = (sc.i_lo + it % nt) * kBM;
       float* dst = p.dq_acc + ((size_t)(b * a.h + hq) * p.lq_pad + q0) * D + dd;
-      bool ok = true;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = warp_wait_parity(&dq_full[h], it & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        uint32_t v[64];
-        tmem_ld32(dq_t + 64 * h, v);
-        tmem_ld32(dq_t + 64 * h + 32, v + 32);
-        tmem_wait_ld();
-        reg_fence<64>(v);
-        tc_fence_before();
-        mbar_arrive(&dq_empty[h]);
-        if (live) {
-          // lanes of a warp hold 32 consecutive head-dim entries of one query row:
-          // each reduction instruction covers one contiguous 128-byte line
+      if (!warp_wait_parity(dq_full, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      uint32_t v[128];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)(64 * h + c) * D, __uint_as_float(v[c]));
-        }
+      for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(dq_t + c0, v + c0);
+      tmem_wait_ld();
+      reg_fence<128>(v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      if (live) {
+        // lanes of a warp hold 32 consecutive head-dim entries of one query row:
+        // each reduction instruction covers one contiguous 128-byte line
+#pragma unroll
+        for (int c = 0; c < 128; ++c) atomicAdd(dst + (size_t)c * D, __uint_as_float(v[c]));
       }
-      if (!ok) break;
     }
   }
 

@@ -42,13 +42,14 @@ constexpr int kThreads = 384;  // 3 warpgroups
 // Register split: launched at kRegsLaunch per thread (65536 / 384 rounded
 // down to 8); the softmax warpgroups raise to kRegsSoftmax and the
 // producer/MMA warpgroup lowers to kRegsOther, which sums to the launch:
-// 256 * 208 + 128 * 88 = 384 * 168.
+// 256 * 200 + 128 * 104 = 384 * 168.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsSoftmax = 208;
-constexpr int kRegsOther = 88;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch, "register split");
-constexpr int kProducerWarp = 8;
+constexpr int kProducerWarp = 8;  // Q and K loads
 constexpr int kMmaWarp = 9;
+constexpr int kVLoadWarp = 10;    // V loads
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 template <int D>
@@ -60,7 +61,7 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + kSub * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 3 * kStages + 3 * kSub + 1;
+  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kSub + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
@@ -105,8 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + C::kStages;
-  uint64_t* kv_empty = v_full + C::kStages;
-  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* k_empty = v_full + C::kStages;  // K and V rings are released separately:
+  uint64_t* v_empty = k_empty + C::kStages; // K_j after the S of tile j, V_j after its P V
+  uint64_t* s_full = v_empty + C::kStages;
   uint64_t* p_full = s_full + kSub;
   uint64_t* o_full = p_full + kSub;
   uint64_t* mma_done = o_full + kSub;
@@ -144,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int t = 0; t < kSub; ++t) {
       mbar_init(&s_full[t], 1);
@@ -189,29 +192,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = sc.lo_all; j < sc.hi_all; ++j, ++it) {
         const int s = it % C::kStages;
         if (it >= C::kStages) {
-          if (!wait_parity(&kv_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, p.status)) break;
+          if (!wait_parity(&k_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, p.status)) break;
         }
         uint8_t* kd = smem + C::kKOff + s * C::kTileBytes;
-        uint8_t* vd = smem + C::kVOff + s * C::kTileBytes;
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d_hint(kd + x * 16384, &tk, &k_full[s], x * 64, kvh, j * kBlockN, b, pol);
-        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d_hint(vd + x * 16384, &tv, &v_full[s], x * 64, kvh, j * kBlockN, b, pol);
       }
       // Loads still in flight must land before the CTA's shared memory goes away.
       const int issued = it;
       for (int k = max(0, issued - C::kStages); k < issued; ++k) {
-        const int s = k % C::kStages;
-        const uint32_t par = (k / C::kStages) & 1;
         volatile int no_abort = 0;
-        wait_parity(&k_full[s], par, &no_abort, p.status, 200000000ull);
-        wait_parity(&v_full[s], par, &no_abort, p.status, 200000000ull);
+        wait_parity(&k_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, p.status, 200000000ull);
       }
       if (qbytes) {
         volatile int no_abort = 0;
         wait_parity(q_full, 0, &no_abort, p.status, 200000000ull);
+      }
+    }
+  } else if (warp == kVLoadWarp) {
+    // ========================== V loads (own ring, own release) ==========================
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      int it = 0;
+      for (int j = sc.lo_all; j < sc.hi_all; ++j, ++it) {
+        const int s = it % C::kStages;
+        if (it >= C::kStages) {
+          if (!wait_parity(&v_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, p.status)) break;
+        }
+        uint8_t* vd = smem + C::kVOff + s * C::kTileBytes;
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d_hint(vd + x * 16384, &tv, &v_full[s], x * 64, kvh, j * kBlockN, b, pol);
+      }
+      const int issued = it;
+      for (int k = max(0, issued - C::kStages); k < issued; ++k) {
+        volatile int no_abort = 0;
+        wait_parity(&v_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, p.status, 200000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -252,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (lo0 == lo_all && hi0 > lo0) BEA_ISSUE_S(0, 0);
           if (lo1 == lo_all && hi1 > lo1) BEA_ISSUE_S(1, 0);
+          umma_commit(&k_empty[0]);  // K of the first tile is read by nothing else
         }
         int it = 0;
         for (int j = lo_all; ok && j < hi_all; ++j, ++it) {
@@ -288,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             BEA_ISSUE_S(1, s1);
           }
-          umma_commit(&kv_empty[s]);
+          if (j + 1 < hi_all) umma_commit(&k_empty[s1]);  // every S of tile j+1 is issued
+          umma_commit(&v_empty[s]);                       // every P V of tile j is issued
           if (j == hi0 - 1) umma_commit(&o_full[0]);
           if (j == hi1 - 1) umma_commit(&o_full[1]);
         }
