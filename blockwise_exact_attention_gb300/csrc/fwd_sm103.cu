@@ -10,9 +10,9 @@
 //
 // One CTA owns 256 query rows (two 128-row subtiles) of one (batch, head):
 //   warp 8      TMA producer: Q once, then K_j / V_j into an NS-stage ring;
-//   warp 9      MMA issuer (one lane): S_t = Q_t K_j^T into TMEM (both
-//               operands in shared memory), O_t += P_t V_j with P_t read
-//               from TMEM;
+//   warp 9      MMA issuer (the whole warp runs the loop, one elected lane
+//               issues): S_t = Q_t K_j^T into TMEM (both operands in
+//               shared memory), O_t += P_t V_j with P_t read from TMEM;
 //   warps 0-3   softmax for subtile 0, warps 4-7 for subtile 1: one thread
 //               per query row (TMEM lane), online softmax, P written back to
 //               TMEM over S as packed bf16, O rescaled in TMEM only when the
@@ -233,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ========================== MMA issuer ==========================
-    if (lane == 0) {
+    // All 32 lanes run the loop and wait together; the issue calls elect one
+    // lane. (With lane 0 alone in the loop, the busy softmax warps on the
+    // same scheduler starve it of issue slots and the tensor core idles.)
+    {
       // base descriptors; every operand below is an offset from one of them
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
       const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
@@ -249,27 +252,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t kd_ = sdesc_add(k_desc, (stg) * C::kTileBytes);                                   \
     _Pragma("unroll") for (int k_ = 0; k_ < D / 16; ++k_) {                                          \
       const uint32_t off_ = (k_ / 4) * 16384 + (k_ % 4) * 32;                                        \
-      umma_ss(tmem + (t) * 128, sdesc_add(qd_, off_), sdesc_add(kd_, off_), C::kIdescS, k_ > 0 ? 1u : 0u); \
+      umma_ss_warp(tmem + (t) * 128, sdesc_add(qd_, off_), sdesc_add(kd_, off_), C::kIdescS, k_ > 0 ? 1u : 0u); \
     }                                                                                                \
-    umma_commit(&s_full[t]);                                                                         \
+    umma_commit_warp(&s_full[t]);                                                                         \
   } while (0)
 // O_t (+)= P_t V from V stage `stg`; P_t is read from TMEM over S_t
 #define BEA_ISSUE_PV(t, stg, first)                                                                  \
   do {                                                                                               \
     const uint64_t vd_ = sdesc_add(v_desc, (stg) * C::kTileBytes);                                   \
     _Pragma("unroll") for (int k_ = 0; k_ < kBlockN / 16; ++k_)                                      \
-      umma_ts(tmem + 256 + (t) * 128, tmem + (t) * 128 + k_ * 8, sdesc_add(vd_, k_ * 2048), C::kIdescPV, \
+      umma_ts_warp(tmem + 256 + (t) * 128, tmem + (t) * 128 + k_ * 8, sdesc_add(vd_, k_ * 2048), C::kIdescPV, \
               (k_ > 0 || !(first)) ? 1u : 0u);                                                       \
   } while (0)
 
       if (hi_all > lo_all) {
-        ok = wait_parity(q_full, 0, abort_flag, p.status);
-        if (ok) ok = wait_parity(&k_full[0], 0, abort_flag, p.status);
+        ok = warp_wait_parity(q_full, 0, abort_flag, p.status);
+        if (ok) ok = warp_wait_parity(&k_full[0], 0, abort_flag, p.status);
         if (ok) {
           tc_fence_after();
           if (lo0 == lo_all && hi0 > lo0) BEA_ISSUE_S(0, 0);
           if (lo1 == lo_all && hi1 > lo1) BEA_ISSUE_S(1, 0);
-          umma_commit(&k_empty[0]);  // K of the first tile is read by nothing else
+          umma_commit_warp(&k_empty[0]);  // K of the first tile is read by nothing else
         }
         int it = 0;
         for (int j = lo_all; ok && j < hi_all; ++j, ++it) {
@@ -280,44 +283,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool a0 = j >= lo0 && j < hi0, a1 = j >= lo1 && j < hi1;
           const bool n0 = j + 1 >= lo0 && j + 1 < hi0, n1 = j + 1 >= lo1 && j + 1 < hi1;
           bool k_next_ready = false;
-          if (!(ok = wait_parity(&v_full[s], par, abort_flag, p.status))) break;
+          if (!(ok = warp_wait_parity(&v_full[s], par, abort_flag, p.status))) break;
           if (a0) {
-            if (!(ok = wait_parity(&p_full[0], pv0 & 1, abort_flag, p.status))) break;
+            if (!(ok = warp_wait_parity(&p_full[0], pv0 & 1, abort_flag, p.status))) break;
             tc_fence_after();
             BEA_ISSUE_PV(0, s, pv0 == 0);
             ++pv0;
           }
           if (n0) {
-            if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
+            if (!(ok = warp_wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
             tc_fence_after();
             k_next_ready = true;
             BEA_ISSUE_S(0, s1);
           }
           if (a1) {
-            if (!(ok = wait_parity(&p_full[1], pv1 & 1, abort_flag, p.status))) break;
+            if (!(ok = warp_wait_parity(&p_full[1], pv1 & 1, abort_flag, p.status))) break;
             tc_fence_after();
             BEA_ISSUE_PV(1, s, pv1 == 0);
             ++pv1;
           }
           if (n1) {
             if (!k_next_ready) {
-              if (!(ok = wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
+              if (!(ok = warp_wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
               tc_fence_after();
             }
             BEA_ISSUE_S(1, s1);
           }
-          if (j + 1 < hi_all) umma_commit(&k_empty[s1]);  // every S of tile j+1 is issued
-          umma_commit(&v_empty[s]);                       // every P V of tile j is issued
-          if (j == hi0 - 1) umma_commit(&o_full[0]);
-          if (j == hi1 - 1) umma_commit(&o_full[1]);
+          if (j + 1 < hi_all) umma_commit_warp(&k_empty[s1]);  // every S of tile j+1 is issued
+          umma_commit_warp(&v_empty[s]);                       // every P V of tile j is issued
+          if (j == hi0 - 1) umma_commit_warp(&o_full[0]);
+          if (j == hi1 - 1) umma_commit_warp(&o_full[1]);
         }
       }
 #undef BEA_ISSUE_S
 #undef BEA_ISSUE_PV
       // Everything issued must finish before TMEM is released.
-      umma_commit(mma_done);
+      umma_commit_warp(mma_done);
       volatile int no_abort = 0;
       wait_parity(mma_done, 0, &no_abort, p.status, 200000000ull);
+      __syncwarp();
     }
   }
   } else {
