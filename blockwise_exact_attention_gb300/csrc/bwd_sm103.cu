@@ -17,7 +17,8 @@
 //      query tiles the causal/window band lets it see:
 //        warp 8      producer: K, V once; per tile Q_i and dO_i (TMA) and the
 //                    tile's L2 and D rows (bulk copies) into 2 stages,
-//        warp 9      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM;
+//        warp 9      MMA issuer (the whole warp, one elected lane issues):
+//                    S^T = K Q_i^T and dP^T = V dO_i^T into TMEM;
 //                    then, per 64-query half as soon as it is ready,
 //                    dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i and
 //                    dQ_i^T = K^T dS^T (dS^T from shared memory),
@@ -356,7 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ========================== MMA issuer ==========================
-    if (lane == 0) {
+    // All 32 lanes run the loop and wait together; the issue calls elect one
+    // lane (a lone issuing lane loses issue slots to the busy compute warps
+    // on its scheduler and feeds the tensor core late).
+    {
       // base descriptors (K-major: LBO unused; MN-major: 64-element blocks 16 KB apart)
       const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
       const uint64_t k_mn = sdesc_sw128(smem_u32(smem + C::kKOff), 16384, 1024);
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16384, 1024);
       const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + C::kDOOff), 16, 1024);
       const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + C::kDOOff), 16384, 1024);
-      bool ok = sc.n_iter > 0 && wait_parity(kv_full, 0, abort_flag, p.status);
+      bool ok = sc.n_iter > 0 && warp_wait_parity(kv_full, 0, abort_flag, p.status);
       for (int it = 0; ok && it < sc.n_iter; ++it) {
         const int s = it & 1;
         const uint32_t par = (it >> 1) & 1;
@@ -375,39 +379,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t q_mn = sdesc_add(q_mn0, s * C::kTileBytes);
         const uint64_t do_kmaj = sdesc_add(do_kmaj0, s * C::kTileBytes);
         const uint64_t do_mn = sdesc_add(do_mn0, s * C::kTileBytes);
-        if (!(ok = wait_parity(&q_full[s], par, abort_flag, p.status))) break;
+        if (!(ok = warp_wait_parity(&q_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
         // S^T = K Q^T   (M = keys, N = 128 queries, K = d; both K-major)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + T_S, sdesc_add(k_kmaj, off), sdesc_add(q_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
+          umma_ss_warp(tmem + T_S, sdesc_add(k_kmaj, off), sdesc_add(q_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
         }
         if (it > 0) {
           // dQ^T of the previous iteration occupies the dP^T columns until read out
-          if (!(ok = wait_parity(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
+          if (!(ok = warp_wait_parity(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
         }
-        if (!(ok = wait_parity(&do_full[s], par, abort_flag, p.status))) break;
+        if (!(ok = warp_wait_parity(&do_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
         // dP^T = V dO^T
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss(tmem + T_DP, sdesc_add(v_kmaj, off), sdesc_add(do_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
+          umma_ss_warp(tmem + T_DP, sdesc_add(v_kmaj, off), sdesc_add(do_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
         }
-        umma_commit(sp_full);
+        umma_commit_warp(sp_full);
         for (int h = 0; h < 2; ++h) {
-          if (!(ok = wait_parity(&ready[h], it & 1, abort_flag, p.status))) break;
+          if (!(ok = warp_wait_parity(&ready[h], it & 1, abort_flag, p.status))) break;
           tc_fence_after();
           // dV += P^T dO over queries [64h, 64h+64)   (A = P^T from TMEM, B = dO MN-major)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_ts(tmem + T_DV, tmem + T_S + (4 * h + k) * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
+            umma_ts_warp(tmem + T_DV, tmem + T_S + (4 * h + k) * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
                     (it > 0 || h > 0 || k > 0) ? 1u : 0u);
           // dK += dS^T Q over the same queries        (A = dS^T K-major, B = Q MN-major)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
+            umma_ss_warp(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
                     C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
         }
         if (!ok) break;
@@ -415,14 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MN-major, B = dS^T MN-major), into the dP^T columns
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          umma_ss(tmem + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, k * 2048), C::kIdescQ, k > 0 ? 1u : 0u);
-        umma_commit(dq_full);
-        umma_commit(&qdo_empty[s]);
+          umma_ss_warp(tmem + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, k * 2048), C::kIdescQ, k > 0 ? 1u : 0u);
+        umma_commit_warp(dq_full);
+        umma_commit_warp(&qdo_empty[s]);
       }
-      if (ok && sc.n_iter > 0) umma_commit(dkv_full);
-      umma_commit(mma_done);
+      if (ok && sc.n_iter > 0) umma_commit_warp(dkv_full);
+      umma_commit_warp(mma_done);
       volatile int no_abort = 0;
       wait_parity(mma_done, 0, &no_abort, p.status, 200000000ull);
+      __syncwarp();
     }
   }
   } else if (warp < 4) {
