@@ -14,26 +14,31 @@
 //      dQ accumulator rows zeroed;
 //   2. main: one CTA per (128-key block, batch, K/V head). K and V stay in
 //      shared memory; the CTA walks the group's query heads x the 128-row
-//      query tiles the causal/window band lets it see:
+//      query tiles the causal/window band lets it see, each tile as two
+//      64-query halves:
 //        warp 8      producer: K, V once; per tile Q_i and dO_i (TMA) and the
 //                    tile's L2 and D rows (bulk copies) into 2 stages,
 //        warp 9      MMA issuer (the whole warp, one elected lane issues):
-//                    S^T = K Q_i^T and dP^T = V dO_i^T into TMEM;
-//                    then, per 64-query half as soon as it is ready,
-//                    dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i and
-//                    dQ_i^T = K^T dS^T (dS^T from shared memory),
-//        warps 0-3   one thread per key: P^T and dS^T from S^T, dP^T, L2, D,
-//                    one 64-query half at a time; finally the dK/dV epilogue,
-//        warps 4-7   one thread per head-dim index: read dQ_i^T out of TMEM
+//                    per half h, S_h^T = K Q_h^T and dP_h^T = V dO_h^T into
+//                    TMEM slot h; then, per half as soon as its P^T / dS^T
+//                    are ready, dV += P_h^T dO_h (P^T from TMEM),
+//                    dK += dS_h^T Q_h and dQ_h^T = K^T dS_h^T (dS^T from
+//                    shared memory),
+//        warps 0-3   one thread per key: P^T and dS^T of one half from S^T,
+//                    dP^T, L2, D; finally the dK/dV epilogue,
+//        warps 4-7   one thread per head-dim index: read dQ_h^T out of TMEM
 //                    and add it into the fp32 accumulator; the 32 lanes of a
 //                    warp cover 32 consecutive entries of a query row, so each
 //                    reduction instruction is one contiguous 128-byte line.
-//      dK and dV accumulate in TMEM across the whole group: no atomics.
+//      Two TMEM slots let the tensor core compute one half while the key
+//      warps work on the other, and the drain of one half's dQ^T overlaps
+//      the other half's products. dK and dV accumulate in TMEM across the
+//      whole group: no atomics.
 //   3. convert: dQ = scale * accumulator, cast or added into the caller's dq.
 //
-// TMEM (512 columns): S^T [0,128) (P^T packed bf16 over its first 64
-// columns), dP^T [128,256) (later dQ^T, 64 columns per query half),
-// dV [256,256+D), dK [384,384+D).
+// TMEM (512 columns): slot h = [128h, 128h+128) holds S_h^T in its first 64
+// columns (P_h^T packed bf16 over the first 32 of them) and dP_h^T in the
+// last 64 (later dQ_h^T); dV [256,256+D), dK [384,384+D).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -69,12 +74,12 @@ struct BwdCfg {
   static constexpr int kDSBytes = 128 * 128 * 2;
   static constexpr int kRowOff = kDSOff + kDSBytes;         // 2 stages of L2[128], D[128] fp32
   static constexpr int kBarOff = kRowOff + 2 * 1024;
-  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 1 + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort*/;
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);    // S_h^T, dP_h^T
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, false, true);     // dV (TMEM A), dK
-  // dQ^T = K^T dS^T: M = 128 head-dim rows (for d = 64 the upper half are padding rows), N = 128 queries
-  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 128, true, true);
+  // dQ_h^T = K^T dS_h^T: M = 128 head-dim rows (for d = 64 the upper half are padding rows), N = 64 queries
+  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -200,7 +205,7 @@ __device__ __forceinline__ bool bwd_tile_needs_mask(const AttnDims& a, int k0, i
 template <int D, bool kMask>
 __device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv, const float* l2s, const float* dds,
                                           int cc, const AttnDims& a, int kj, int q0, float scale_log2,
-                                          uint32_t s_t, uint8_t* ds_row, int j) {
+                                          uint32_t p_dst, uint8_t* ds_row, int j) {
   uint32_t pk[16], dk[16];
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
@@ -227,7 +232,7 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv
     dk[e4 * 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
   }
   // P^T (packed bf16 pairs) over S^T columns that this thread has already read
-  tmem_st16(s_t + cc * 16, pk);
+  tmem_st16(p_dst, pk);
   // dS^T row j, queries [32cc, 32cc+32): 4 chunks of 16 B, 128-byte swizzle
   uint8_t* half = ds_row + (cc >> 1) * 16384;
 #pragma unroll
@@ -250,11 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 1;        // Q_i, L2_i, D_i of a stage
   uint64_t* do_full = q_full + 2;
   uint64_t* qdo_empty = do_full + 2;
-  uint64_t* sp_full = qdo_empty + 2;  // S^T and dP^T of an iteration are in TMEM
-  uint64_t* ready = sp_full + 1;      // [2]: P^T / dS^T of query half h written
-  uint64_t* dq_full = ready + 2;      // dQ^T of the tile in TMEM
-  uint64_t* dq_empty = dq_full + 1;   // dQ^T of the tile read out
-  uint64_t* dkv_full = dq_empty + 1;
+  uint64_t* sp_full = qdo_empty + 2;  // [2]: S_h^T and dP_h^T of half h are in TMEM slot h
+  uint64_t* ready = sp_full + 2;      // [2]: P_h^T / dS_h^T written
+  uint64_t* dq_full = ready + 2;      // [2]: dQ_h^T in TMEM slot h
+  uint64_t* dq_empty = dq_full + 2;   // [2]: dQ_h^T read out of slot h
+  uint64_t* dkv_full = dq_empty + 2;
   uint64_t* mma_done = dkv_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -299,10 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&do_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
       mbar_init(&ready[s], 128);
+      mbar_init(&sp_full[s], 1);
+      mbar_init(&dq_full[s], 1);
+      mbar_init(&dq_empty[s], 128);
     }
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
-    mbar_init(sp_full, 1);
     mbar_init(dkv_full, 1);
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -315,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384;
+  // TMEM slot h: S_h^T at 128h (P_h^T over its first 32 columns), dP_h^T / dQ_h^T at 128h + 64
+  const uint32_t T_DP = 64, T_DV = 256, T_DK = 384;
 
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
@@ -381,46 +387,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t do_mn = sdesc_add(do_mn0, s * C::kTileBytes);
         if (!(ok = warp_wait_parity(&q_full[s], par, abort_flag, p.status))) break;
         tc_fence_after();
-        // S^T = K Q^T   (M = keys, N = 128 queries, K = d; both K-major)
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss_warp(tmem + T_S, sdesc_add(k_kmaj, off), sdesc_add(q_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
-        }
-        if (it > 0) {
-          // dQ^T of the previous iteration occupies the dP^T columns until read out
-          if (!(ok = warp_wait_parity(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
-        }
-        if (!(ok = warp_wait_parity(&do_full[s], par, abort_flag, p.status))) break;
-        tc_fence_after();
-        // dP^T = V dO^T
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss_warp(tmem + T_DP, sdesc_add(v_kmaj, off), sdesc_add(do_kmaj, off), C::kIdescS, k > 0 ? 1u : 0u);
-        }
-        umma_commit_warp(sp_full);
         for (int h = 0; h < 2; ++h) {
+          const uint32_t slot = tmem + 128u * h;
+          // S_h^T = K Q_h^T   (M = keys, N = 64 queries, K = d; both K-major). It overwrites
+          // P_h^T of the previous tile, which that tile's dV product (issued earlier) consumed.
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+            umma_ss_warp(slot, sdesc_add(k_kmaj, off), sdesc_add(q_kmaj, h * 8192 + off), C::kIdescS,
+                         k > 0 ? 1u : 0u);
+          }
+          // dQ_h^T of the previous tile occupies the dP_h^T columns until the drain has read it
+          if (it > 0 && !(ok = warp_wait_parity(&dq_empty[h], (it - 1) & 1, abort_flag, p.status))) break;
+          if (h == 0 && !(ok = warp_wait_parity(&do_full[s], par, abort_flag, p.status))) break;
+          tc_fence_after();
+          // dP_h^T = V dO_h^T
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+            umma_ss_warp(slot + T_DP, sdesc_add(v_kmaj, off), sdesc_add(do_kmaj, h * 8192 + off), C::kIdescS,
+                         k > 0 ? 1u : 0u);
+          }
+          umma_commit_warp(&sp_full[h]);
+        }
+        if (!ok) break;
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t slot = tmem + 128u * h;
           if (!(ok = warp_wait_parity(&ready[h], it & 1, abort_flag, p.status))) break;
           tc_fence_after();
-          // dV += P^T dO over queries [64h, 64h+64)   (A = P^T from TMEM, B = dO MN-major)
+          // dV += P_h^T dO_h   (A = P_h^T from TMEM, B = dO MN-major)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_ts_warp(tmem + T_DV, tmem + T_S + (4 * h + k) * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
-                    (it > 0 || h > 0 || k > 0) ? 1u : 0u);
-          // dK += dS^T Q over the same queries        (A = dS^T K-major, B = Q MN-major)
+            umma_ts_warp(tmem + T_DV, slot + k * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
+                         (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+          // dK += dS_h^T Q_h    (A = dS^T K-major, B = Q MN-major)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             umma_ss_warp(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
-                    C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+                         C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
+          // dQ_h^T = K^T dS_h^T  (A = K read MN-major, B = dS_h^T MN-major), into the dP_h^T columns
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            umma_ss_warp(slot + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048), C::kIdescQ,
+                         k > 0 ? 1u : 0u);
+          umma_commit_warp(&dq_full[h]);
         }
         if (!ok) break;
-        // dQ^T = K^T dS^T over all 128 queries in one N = 128 product (A = K read
-        // MN-major, B = dS^T MN-major), into the dP^T columns
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          umma_ss_warp(tmem + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, k * 2048), C::kIdescQ, k > 0 ? 1u : 0u);
-        umma_commit_warp(dq_full);
         umma_commit_warp(&qdo_empty[s]);
       }
       if (ok && sc.n_iter > 0) umma_commit_warp(dkv_full);
@@ -436,41 +448,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = threadIdx.x;  // key row == TMEM lane
     const int kj = sc.k0 + j;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t s_t = tmem + lane_base + T_S;
-    const uint32_t dp_t = tmem + lane_base + T_DP;
     uint8_t* ds_row = smem + C::kDSOff + j * 128;
     bool ok = true;
-    for (int it = 0; it < sc.n_iter; ++it) {
+    for (int it = 0; ok && it < sc.n_iter; ++it) {
       const int s = it & 1;
       const int q0 = (sc.i_lo + it % nt) * kBM;
-      // S^T, dP^T of this iteration; it also means every MMA of the previous
-      // iteration (the readers of the dS^T buffer and of P^T) has completed
-      if (!(ok = warp_wait_parity(sp_full, it & 1, abort_flag, p.status))) break;
-      tc_fence_after();
       const bool need_mask = bwd_tile_needs_mask(a, sc.k0, q0);
       const float* l2s = reinterpret_cast<const float*>(smem + C::kRowOff + s * 1024);
       const float* dds = l2s + kBM;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
+        // S_h^T, dP_h^T of this tile; this also means every MMA issued before
+        // them (the previous readers of the dS^T half and of P_h^T) has completed
+        if (!(ok = warp_wait_parity(&sp_full[h], it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        const uint32_t slot = tmem + lane_base + 128u * h;
         uint32_t sv0[32], pv0[32], sv1[32], pv1[32];
-        tmem_ld32(s_t + 64 * h, sv0);
-        tmem_ld32(dp_t + 64 * h, pv0);
+        tmem_ld32(slot, sv0);
+        tmem_ld32(slot + T_DP, pv0);
         tmem_wait_ld();
         reg_fence<32>(sv0);
         reg_fence<32>(pv0);
-        tmem_ld32(s_t + 64 * h + 32, sv1);  // in flight while chunk 2h is processed
-        tmem_ld32(dp_t + 64 * h + 32, pv1);
+        tmem_ld32(slot + 32, sv1);  // in flight while chunk 2h is processed
+        tmem_ld32(slot + T_DP + 32, pv1);
         if (need_mask)
-          bwd_chunk<D, true>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, s_t, ds_row, j);
+          bwd_chunk<D, true>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, slot, ds_row, j);
         else
-          bwd_chunk<D, false>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, s_t, ds_row, j);
+          bwd_chunk<D, false>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, slot, ds_row, j);
         tmem_wait_ld();
         reg_fence<32>(sv1);
         reg_fence<32>(pv1);
         if (need_mask)
-          bwd_chunk<D, true>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, s_t, ds_row, j);
+          bwd_chunk<D, true>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, slot + 16, ds_row, j);
         else
-          bwd_chunk<D, false>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, s_t, ds_row, j);
+          bwd_chunk<D, false>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, slot + 16, ds_row, j);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
@@ -541,26 +552,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ========================== dQ drain (one thread per head-dim index) ==========================
     const int dd = threadIdx.x - 128;  // dQ^T row == head-dim index == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-    const uint32_t dq_t = tmem + lane_base + T_DP;
     const bool live = dd < D;  // for d = 64 the upper 64 lanes hold padding rows
-    for (int it = 0; it < sc.n_iter; ++it) {
+    bool ok = true;
+    for (int it = 0; ok && it < sc.n_iter; ++it) {
       const int hq = kvh * sc.g + it / nt;
       const int q0 = (sc.i_lo + it % nt) * kBM;
-      float* dst = p.dq_acc + ((size_t)(b * a.h + hq) * p.lq_pad + q0) * D + dd;
-      if (!warp_wait_parity(dq_full, it & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      uint32_t v[128];
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float* dst = p.dq_acc + ((size_t)(b * a.h + hq) * p.lq_pad + q0 + 64 * h) * D + dd;
+        if (!(ok = warp_wait_parity(&dq_full[h], it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        uint32_t v[64];
+        const uint32_t dq_t = tmem + lane_base + 128u * h + T_DP;
+        tmem_ld32(dq_t, v);
+        tmem_ld32(dq_t + 32, v + 32);
+        tmem_wait_ld();
+        reg_fence<64>(v);
+        tc_fence_before();
+        mbar_arrive(&dq_empty[h]);
+        if (live) {
+          // lanes of a warp hold 32 consecutive head-dim entries of one query row:
+          // each reduction instruction covers one contiguous 128-byte line
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(dq_t + c0, v + c0);
-      tmem_wait_ld();
-      reg_fence<128>(v);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      if (live) {
-        // lanes of a warp hold 32 consecutive head-dim entries of one query row:
-        // each reduction instruction covers one contiguous 128-byte line
-#pragma unroll
-        for (int c = 0; c < 128; ++c) atomicAdd(dst + (size_t)c * D, __uint_as_float(v[c]));
+          for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)c * D, __uint_as_float(v[c]));
+        }
       }
     }
   }
