@@ -23,7 +23,10 @@
 //                    TMEM slot h; then, per half as soon as its P^T / dS^T
 //                    are ready, dV += P_h^T dO_h (P^T from TMEM),
 //                    dK += dS_h^T Q_h and dQ_h^T = K^T dS_h^T (dS^T from
-//                    shared memory),
+//                    shared memory). The next tile's first-half S^T / dP^T
+//                    are issued ahead of this tile's second-half gradient
+//                    products, so the key warps never wait for a whole tile
+//                    of tensor work,
 //        warps 0-3   one thread per key: P^T and dS^T of one half from S^T,
 //                    dP^T, L2, D; finally the dK/dV epilogue,
 //        warps 4-7   one thread per head-dim index: read dQ_h^T out of TMEM
@@ -53,11 +56,11 @@ constexpr int kThreads = 384;  // 3 warpgroups
 // Register split: launched at kRegsLaunch per thread (65536 / 384 rounded
 // down to 8); the key-row warpgroup rises to kRegsCompute, the dQ drain and
 // the producer/MMA warpgroup drop to kRegsDrain and kRegsOther:
-// 128 * (224 + 160 + 120) = 384 * 168.
+// 128 * (224 + 128 + 152) = 384 * 168.
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsCompute = 224;
-constexpr int kRegsDrain = 160;
-constexpr int kRegsOther = 120;
+constexpr int kRegsDrain = 128;
+constexpr int kRegsOther = 152;
 static_assert(kRegsCompute + kRegsDrain + kRegsOther == 3 * kRegsLaunch, "register split");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -377,63 +380,94 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16384, 1024);
       const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + C::kDOOff), 16, 1024);
       const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + C::kDOOff), 16384, 1024);
+      // S_h^T = K Q_h^T (M = keys, N = 64 queries, K = d; both K-major) into slot h. It
+      // overwrites P_h^T of the previous tile, which that tile's dV product (issued
+      // earlier) consumed.
+      auto issue_s = [&](int h, int st) {
+        const uint64_t qd = sdesc_add(q_kmaj0, st * C::kTileBytes + h * 8192);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          umma_ss_warp(tmem + 128u * h, sdesc_add(k_kmaj, off), sdesc_add(qd, off), C::kIdescS, k > 0 ? 1u : 0u);
+        }
+      };
+      // dP_h^T = V dO_h^T into the second half of slot h (where dQ_h^T of the previous tile
+      // was: the caller has waited for the drain)
+      auto issue_dp = [&](int h, int st) {
+        const uint64_t dd = sdesc_add(do_kmaj0, st * C::kTileBytes + h * 8192);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(v_kmaj, off), sdesc_add(dd, off), C::kIdescS,
+                       k > 0 ? 1u : 0u);
+        }
+      };
+      // dV += P_h^T dO_h (A = P_h^T from TMEM, B = dO MN-major); dK += dS_h^T Q_h (A = dS^T
+      // K-major, B = Q MN-major); dQ_h^T = K^T dS_h^T (A = K read MN-major, B = dS_h^T
+      // MN-major) into the second half of slot h
+      auto issue_grads = [&](int h, int st, bool first) {
+        const uint64_t q_mn = sdesc_add(q_mn0, st * C::kTileBytes);
+        const uint64_t do_mn = sdesc_add(do_mn0, st * C::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ts_warp(tmem + T_DV, tmem + 128u * h + k * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
+                       (!first || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss_warp(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
+                       C::kIdescKV, (!first || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048),
+                       C::kIdescQ, k > 0 ? 1u : 0u);
+      };
+      // Issue order: S_0 dP_0 S_1 dP_1 (tile 0), then per tile i
+      //   [P_0/dS_0 ready] grads_0(i)
+      //   [P_1/dS_1 ready] S_0 dP_0 (tile i+1), grads_1(i), S_1 dP_1 (tile i+1)
+      // so that the key warps can start on tile i+1 while the tensor core finishes tile i.
       bool ok = sc.n_iter > 0 && warp_wait_parity(kv_full, 0, abort_flag, p.status);
-      for (int it = 0; ok && it < sc.n_iter; ++it) {
-        const int s = it & 1;
-        const uint32_t par = (it >> 1) & 1;
-        const uint64_t q_kmaj = sdesc_add(q_kmaj0, s * C::kTileBytes);
-        const uint64_t q_mn = sdesc_add(q_mn0, s * C::kTileBytes);
-        const uint64_t do_kmaj = sdesc_add(do_kmaj0, s * C::kTileBytes);
-        const uint64_t do_mn = sdesc_add(do_mn0, s * C::kTileBytes);
-        if (!(ok = warp_wait_parity(&q_full[s], par, abort_flag, p.status))) break;
+      if (ok) ok = warp_wait_parity(&q_full[0], 0, abort_flag, p.status);
+      if (ok) ok = warp_wait_parity(&do_full[0], 0, abort_flag, p.status);
+      if (ok) {
         tc_fence_after();
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t slot = tmem + 128u * h;
-          // S_h^T = K Q_h^T   (M = keys, N = 64 queries, K = d; both K-major). It overwrites
-          // P_h^T of the previous tile, which that tile's dV product (issued earlier) consumed.
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-            umma_ss_warp(slot, sdesc_add(k_kmaj, off), sdesc_add(q_kmaj, h * 8192 + off), C::kIdescS,
-                         k > 0 ? 1u : 0u);
-          }
-          // dQ_h^T of the previous tile occupies the dP_h^T columns until the drain has read it
-          if (it > 0 && !(ok = warp_wait_parity(&dq_empty[h], (it - 1) & 1, abort_flag, p.status))) break;
-          if (h == 0 && !(ok = warp_wait_parity(&do_full[s], par, abort_flag, p.status))) break;
+        issue_s(0, 0);
+        issue_dp(0, 0);
+        umma_commit_warp(&sp_full[0]);
+        issue_s(1, 0);
+        issue_dp(1, 0);
+        umma_commit_warp(&sp_full[1]);
+      }
+      for (int it = 0; ok && it < sc.n_iter; ++it) {
+        const int s = it & 1, s1 = s ^ 1;
+        const uint32_t par1 = ((it + 1) >> 1) & 1;
+        const bool more = it + 1 < sc.n_iter;
+        if (!(ok = warp_wait_parity(&ready[0], it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        issue_grads(0, s, it == 0);
+        umma_commit_warp(&dq_full[0]);
+        if (!(ok = warp_wait_parity(&ready[1], it & 1, abort_flag, p.status))) break;
+        if (more) {
+          if (!(ok = warp_wait_parity(&q_full[s1], par1, abort_flag, p.status))) break;
           tc_fence_after();
-          // dP_h^T = V dO_h^T
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-            umma_ss_warp(slot + T_DP, sdesc_add(v_kmaj, off), sdesc_add(do_kmaj, h * 8192 + off), C::kIdescS,
-                         k > 0 ? 1u : 0u);
-          }
-          umma_commit_warp(&sp_full[h]);
-        }
-        if (!ok) break;
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t slot = tmem + 128u * h;
-          if (!(ok = warp_wait_parity(&ready[h], it & 1, abort_flag, p.status))) break;
+          issue_s(0, s1);
+          // dQ_0^T of tile i occupies the dP_0^T columns until the drain has read it
+          if (!(ok = warp_wait_parity(&dq_empty[0], it & 1, abort_flag, p.status))) break;
+          if (!(ok = warp_wait_parity(&do_full[s1], par1, abort_flag, p.status))) break;
           tc_fence_after();
-          // dV += P_h^T dO_h   (A = P_h^T from TMEM, B = dO MN-major)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ts_warp(tmem + T_DV, slot + k * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
-                         (it > 0 || h > 0 || k > 0) ? 1u : 0u);
-          // dK += dS_h^T Q_h    (A = dS^T K-major, B = Q MN-major)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss_warp(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
-                         C::kIdescKV, (it > 0 || h > 0 || k > 0) ? 1u : 0u);
-          // dQ_h^T = K^T dS_h^T  (A = K read MN-major, B = dS_h^T MN-major), into the dP_h^T columns
-#pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            umma_ss_warp(slot + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048), C::kIdescQ,
-                         k > 0 ? 1u : 0u);
-          umma_commit_warp(&dq_full[h]);
+          issue_dp(0, s1);
+          umma_commit_warp(&sp_full[0]);
         }
-        if (!ok) break;
-        umma_commit_warp(&qdo_empty[s]);
+        tc_fence_after();
+        issue_grads(1, s, false);
+        umma_commit_warp(&dq_full[1]);
+        umma_commit_warp(&qdo_empty[s]);  // the last readers of stage s are issued
+        if (more) {
+          issue_s(1, s1);
+          if (!(ok = warp_wait_parity(&dq_empty[1], it & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_dp(1, s1);
+          umma_commit_warp(&sp_full[1]);
+        }
       }
       if (ok && sc.n_iter > 0) umma_commit_warp(dkv_full);
       umma_commit_warp(mma_done);
