@@ -36,6 +36,16 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, causal) and % of GB300 BF16 ten
 WORKLOAD = "causal_gqa_8k_rope"
 L2_FLUSH_BYTES = 256 << 20
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# each kernel on the workloads below, from one `ncu --set full` capture of
+# `bench.py --only {fwd,bwd,merge}`. A kernel changed since its capture gets
+# None here until it is captured again.
+NCU_TRAFFIC_BYTES = {
+    "bwd_bf16_kernel<128>": 655.1e6 + 294.9e6,   # causal GQA 8k, one launch
+    "fwd_bf16_kernel<128>": 100.9e6 + 32.6e6,    # causal GQA 8k, one launch
+    "ring_merge_kernel": 204.1e6 + 76.2e6,       # [1,16384,16,128]; second of back-to-back launches
+}
+
 
 def bench_config(world: int) -> dict:
     return {"workload": "causal GQA bf16 q[1,8192,32,128] k/v[1,8192,8,128], RoPE on host, scale 1/sqrt(128)",
@@ -245,6 +255,16 @@ def main():
     def bwd():
         bea.flash_mha_bwd(do, q, k, v, out, lse, s, True, dq=dq, dk=dk, dv=dv, workspace=ws)
 
+    # The same backward as its three stages (exactly the kernels flash_mha_bwd
+    # launches), with events between them so that the dominant kernel, the
+    # backward main kernel, is timed on its own.
+    def bwd_staged(ev):
+        bea.flash_mha_bwd_prepare(do, out, lse, ws)
+        ev[0].record(stream)
+        bea.flash_mha_bwd_kv_block(do, q, k, v, dk, dv, s, True, workspace=ws)
+        ev[1].record(stream)
+        bea.flash_mha_bwd_finish(dq, s, workspace=ws)
+
     def timed(fn, reps, warm):
         for _ in range(warm):
             fn()
@@ -270,33 +290,36 @@ def main():
     if dist:
         dist.barrier()
     bea.launches_since_reset(reset=True)
-    t_fwd, t_bwd = [], []
+    t_fwd, t_bwd, t_main = [], [], []
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         for _ in range(args.steps):
             flush_l2()
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0, e1, e2, m0, m1 = (torch.cuda.Event(enable_timing=True) for _ in range(5))
             e0.record(stream)
             fwd()
             e1.record(stream)
-            bwd()
+            bwd_staged((m0, m1))
             e2.record(stream)
             e2.synchronize()
             t_fwd.append(e0.elapsed_time(e1))
             t_bwd.append(e1.elapsed_time(e2))
+            t_main.append(m0.elapsed_time(m1))
         torch.cuda.synchronize()
     launches = bea.launches_since_reset(reset=True)
     status = bea.device_status()
     ms_fwd = sum(t_fwd) / len(t_fwd)
     ms_bwd = sum(t_bwd) / len(t_bwd)
+    ms_main = sum(t_main) / len(t_main)
     ms_step = ms_fwd + ms_bwd
     if dist:
-        tt = torch.tensor([ms_step, ms_fwd, ms_bwd], device=dev)
+        tt = torch.tensor([ms_step, ms_fwd, ms_bwd, ms_main], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd, ms_bwd = (float(v_) for v_ in tt)
+        ms_step, ms_fwd, ms_bwd, ms_main = (float(v_) for v_ in tt)
     value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
     fwd_tf = f_fwd / (ms_fwd * 1e-3) / 1e12
     bwd_tf = f_bwd / (ms_bwd * 1e-3) / 1e12
+    main_tf = f_bwd / (ms_main * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ----
     hq_, hk_, hv_, hdo_ = (t.cpu().pin_memory() for t in (q, k, v, do))
@@ -357,7 +380,6 @@ def main():
                "sample": f"fwd+bwd of K/V head 0 (query heads 0..3) of the same workload, all rows, fp64 numpy, "
                          f"{fl:.3e} FLOPs in {sec:.1f} s"}
 
-    bwd_launch_ms = ms_bwd
     line = {
         "metric": METRIC,
         "value": value,
@@ -378,13 +400,18 @@ def main():
         "ms_bwd": ms_bwd,
         "pct_peak": {"fwd": fwd_tf / pk_burst, "bwd": bwd_tf / pk_burst, "fwd_bwd": value / world / pk_burst,
                      "peak_tflops": pk_burst, "peak_kind": f"{pk_kind} bf16 burst"},
-        "roofline": {"bound": "tensor", "kernel": "bwd (preprocess + tcgen05 main + dQ convert, one call)",
-                     "achieved": bwd_tf, "peak": pk_burst, "unit": "TFLOP/s", "frac": bwd_tf / pk_burst,
-                     "traffic": None, "peak_kind": f"{pk_kind} bf16 burst (kernel timed alone per step)"},
-        "roofline_fwd": {"bound": "tensor", "kernel": "fwd_bf16_kernel<128>", "achieved": fwd_tf, "peak": pk_burst,
-                         "unit": "TFLOP/s", "frac": fwd_tf / pk_burst, "traffic": None},
+        # dominant kernel: the backward main kernel (~71% of a step), timed alone with
+        # events around its launch; algorithmic work = the backward's 2.5 x forward FLOPs
+        "roofline": {"bound": "tensor", "kernel": "bwd_bf16_kernel<128>", "ms": ms_main,
+                     "achieved": main_tf, "peak": pk_burst, "unit": "TFLOP/s", "frac": main_tf / pk_burst,
+                     "traffic": NCU_TRAFFIC_BYTES["bwd_bf16_kernel<128>"],
+                     "peak_kind": f"{pk_kind} bf16 burst (a ~2 ms step, L2 flushed before it)"},
+        "roofline_fwd": {"bound": "tensor", "kernel": "fwd_bf16_kernel<128>", "ms": ms_fwd, "achieved": fwd_tf,
+                         "peak": pk_burst, "unit": "TFLOP/s", "frac": fwd_tf / pk_burst,
+                         "traffic": NCU_TRAFFIC_BYTES["fwd_bf16_kernel<128>"]},
         "merge": {"kernel": "ring_merge [1,16384,16,128] f32 acc + bf16 blk", "ms": merge_ms,
-                  "bytes": merge_bytes, "gbs": merge_gbs, "peak_gbs": pk_hbm, "frac": merge_gbs / pk_hbm},
+                  "bytes": merge_bytes, "gbs": merge_gbs, "peak_gbs": pk_hbm, "frac": merge_gbs / pk_hbm,
+                  "bound": "hbm", "traffic": NCU_TRAFFIC_BYTES["ring_merge_kernel"]},
         "ring": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks (36 fwd + 28 merges)", "ms": ring_ms,
                  "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -4,6 +4,8 @@ Public API (all calls run in libbea.so's CUDA kernels on the current stream):
 
 * ``flash_mha_fwd(q, k, v, softmax_scale, is_causal, window_size) -> (out, lse)``
 * ``flash_mha_bwd(dout, q, k, v, out, lse, ...) -> (dq, dk, dv)``
+* ``flash_mha_bwd_prepare / flash_mha_bwd_kv_block / flash_mha_bwd_finish``:
+  the same backward in stages, dQ accumulated over several K/V blocks
 * ``ring_merge(out_acc, lse_acc, out_blk, lse_blk, out_final=None)``
 * ``ring_attention_fwd / ring_attention_bwd``: ring attention replayed as
   chunk steps on one GPU.
@@ -14,6 +16,9 @@ from .ops import (  # noqa: F401
     bwd_workspace_bytes,
     device_status,
     flash_mha_bwd,
+    flash_mha_bwd_finish,
+    flash_mha_bwd_kv_block,
+    flash_mha_bwd_prepare,
     flash_mha_fwd,
     launches_since_reset,
     ring_merge,

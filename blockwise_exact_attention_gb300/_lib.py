@@ -41,6 +41,9 @@ EXPORTS = (
     "bea_selftest_wait_timeout",
     "bea_last_launch_count",
     "bea_flash_mha_bwd_noalloc",
+    "bea_flash_mha_bwd_prepare",
+    "bea_flash_mha_bwd_kv_block",
+    "bea_flash_mha_bwd_finish",
 )
 
 
@@ -94,6 +97,12 @@ def load() -> ctypes.CDLL:
     lib.bea_last_launch_count.restype = i
     lib.bea_flash_mha_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, f, i, i, i, i, vp]
     lib.bea_flash_mha_bwd_noalloc.restype = i
+    lib.bea_flash_mha_bwd_prepare.argtypes = [P, P, P, vp, sz, vp]
+    lib.bea_flash_mha_bwd_prepare.restype = i
+    lib.bea_flash_mha_bwd_kv_block.argtypes = [P, P, P, P, P, P, f, i, i, i, i, vp, sz, vp]
+    lib.bea_flash_mha_bwd_kv_block.restype = i
+    lib.bea_flash_mha_bwd_finish.argtypes = [P, f, i, vp, sz, vp]
+    lib.bea_flash_mha_bwd_finish.restype = i
     _LIB = lib
     return lib
 

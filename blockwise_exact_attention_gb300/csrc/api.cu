@@ -194,6 +194,35 @@ BwdWorkspace bwd_workspace_layout(int64_t n, int64_t lq, int64_t h, int64_t d) {
   return w;
 }
 
+int check_workspace(const void* workspace, size_t workspace_bytes, const BwdWorkspace& w) {
+  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < w.total)
+    return BEA_ERR_WORKSPACE;
+  return BEA_OK;
+}
+
+// Workspace pointers of the bf16 backward stages.
+void set_workspace(bea::BwdParams* p, void* workspace, const BwdWorkspace& w) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p->dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
+  p->d_row = reinterpret_cast<float*>(ws + w.d_off);
+  p->lse2 = reinterpret_cast<float*>(ws + w.l_off);
+  p->lq_pad = (p->a.lq + 127) / 128 * 128;
+}
+
+// Dims of a stage that sees only [n, lq, h, d] query-side tensors (bf16 path).
+int query_side_dims(const bea_tensor* t, AttnDims* a) {
+  const int64_t d = t->shape[3];
+  if (d != 64 && d != 128) return BEA_ERR_UNSUPPORTED;
+  if (t->shape[0] * t->shape[2] > (int64_t(1) << 31) - 1) return BEA_ERR_SHAPE;
+  a->n = (int)t->shape[0];
+  a->lq = a->lk = (int)t->shape[1];
+  a->h = a->hkv = (int)t->shape[2];
+  a->d = (int)d;
+  a->wl = a->wr = -1;
+  a->scale = 1.f;
+  return BEA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -279,8 +308,7 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
   }
   if (f32 && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
   const BwdWorkspace w = bwd_workspace_layout(a.n, a.lq, a.h, a.d);
-  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < w.total)
-    return BEA_ERR_WORKSPACE;
+  if ((rc = check_workspace(workspace, workspace_bytes, w))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
   if (a.n == 0 || a.h == 0) return finish(cudaSuccess, 0);
@@ -304,10 +332,7 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
   p.dv_is_f32 = dv->dtype == BEA_F32;
   p.lse = lse3(lse);
   p.accumulate = accumulate;
-  p.dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
-  p.d_row = reinterpret_cast<float*>(ws + w.d_off);
-  p.lse2 = reinterpret_cast<float*>(ws + w.l_off);
-  p.lq_pad = (a.lq + 127) / 128 * 128;
+  set_workspace(&p, workspace, w);
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
   CUtensorMap tq, tk, tv, tdo;
   std::memset(&tq, 0, sizeof(tq));
@@ -320,6 +345,93 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
       return rc;
   }
   return finish(bea::launch_bwd_bf16(p, tq, tk, tv, tdo, s, &launches), launches);
+}
+
+int bea_flash_mha_bwd_prepare(const bea_tensor* dout, const bea_tensor* out, const bea_tensor* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  int rc;
+  if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(out, 4))) return rc;
+  if (dout->dtype != BEA_BF16) return dout->dtype == BEA_F32 ? BEA_ERR_UNSUPPORTED : BEA_ERR_DTYPE;
+  if (!same_shape(out, dout)) return BEA_ERR_SHAPE;
+  if (out->dtype != BEA_BF16 && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  bea::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((rc = query_side_dims(dout, &p.a))) return rc;
+  if ((rc = check_lse(lse, p.a))) return rc;
+  const BwdWorkspace w = bwd_workspace_layout(p.a.n, p.a.lq, p.a.h, p.a.d);
+  if ((rc = check_workspace(workspace, workspace_bytes, w))) return rc;
+  p.dout = seq4(dout);
+  p.out = seq4(out);
+  p.out_is_f32 = out->dtype == BEA_F32;
+  p.lse = lse3(lse);
+  set_workspace(&p, workspace, w);
+  int launches = 0;
+  return finish(bea::launch_bwd_prepare(p, static_cast<cudaStream_t>(stream), &launches), launches);
+}
+
+int bea_flash_mha_bwd_kv_block(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k,
+                               const bea_tensor* v, const bea_tensor* dk, const bea_tensor* dv,
+                               float softmax_scale, int is_causal, int window_left, int window_right,
+                               int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  AttnDims a;
+  int rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if (q->dtype != BEA_BF16) return BEA_ERR_UNSUPPORTED;
+  if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(dk, 4)) || (rc = check_tensor(dv, 4))) return rc;
+  if (!same_shape(dout, q) || !same_shape(dk, k) || !same_shape(dv, k)) return BEA_ERR_SHAPE;
+  if (dout->dtype != BEA_BF16) return BEA_ERR_DTYPE;
+  if (accumulate != 0 && accumulate != 1) return BEA_ERR_ARG;
+  for (const bea_tensor* g : {dk, dv}) {
+    if (g->dtype != BEA_BF16 && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
+    if (accumulate && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  }
+  const BwdWorkspace w = bwd_workspace_layout(a.n, a.lq, a.h, a.d);
+  if ((rc = check_workspace(workspace, workspace_bytes, w))) return rc;
+  int launches = 0;
+  if (a.n == 0 || a.h == 0) return finish(cudaSuccess, 0);
+  bea::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.a = a;
+  p.dk = seq4(dk);
+  p.dv = seq4(dv);
+  p.dk_is_f32 = dk->dtype == BEA_F32;
+  p.dv_is_f32 = dv->dtype == BEA_F32;
+  p.accumulate = accumulate;
+  set_workspace(&p, workspace, w);
+  if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  std::memset(&tq, 0, sizeof(tq));
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  std::memset(&tdo, 0, sizeof(tdo));
+  if (a.lq > 0 && a.lk > 0) {
+    if ((rc = make_seq_map(q, &tq)) || (rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv)) ||
+        (rc = make_seq_map(dout, &tdo)))
+      return rc;
+  }
+  return finish(bea::launch_bwd_main(p, tq, tk, tv, tdo, static_cast<cudaStream_t>(stream), &launches), launches);
+}
+
+int bea_flash_mha_bwd_finish(const bea_tensor* dq, float softmax_scale, int accumulate, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  int rc;
+  if ((rc = check_tensor(dq, 4))) return rc;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return BEA_ERR_ARG;
+  if (accumulate != 0 && accumulate != 1) return BEA_ERR_ARG;
+  if (dq->dtype != BEA_BF16 && dq->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  if (accumulate && dq->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  bea::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((rc = query_side_dims(dq, &p.a))) return rc;
+  p.a.scale = softmax_scale;
+  const BwdWorkspace w = bwd_workspace_layout(p.a.n, p.a.lq, p.a.h, p.a.d);
+  if ((rc = check_workspace(workspace, workspace_bytes, w))) return rc;
+  p.dq = seq4(dq);
+  p.dq_is_f32 = dq->dtype == BEA_F32;
+  p.accumulate = accumulate;
+  set_workspace(&p, workspace, w);
+  int launches = 0;
+  return finish(bea::launch_bwd_finish(p, static_cast<cudaStream_t>(stream), &launches), launches);
 }
 
 int bea_ring_merge(const bea_tensor* out_acc, const bea_tensor* lse_acc, const bea_tensor* out_blk,

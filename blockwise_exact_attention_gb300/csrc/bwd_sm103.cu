@@ -625,51 +625,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
+cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
   using C = BwdCfg<D>;
   const AttnDims& a = p.a;
-  cudaError_t e;
-  {
-    const int64_t rows = (int64_t)a.n * a.h * p.lq_pad;
-    if (rows > 0) {
-      bwd_preprocess_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
-      *nlaunch += 1;
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-  }
   const int nkb = (a.lk + kBN - 1) / kBN;
   const long long blocks = (long long)nkb * a.n * a.hkv;
-  if (blocks > 0) {
-    e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // The register split is only sound at exactly kRegsLaunch registers per
-    // thread; refuse to launch otherwise (setmaxnreg.inc would never return).
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D>);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-    const float scale_log2 = a.scale * 1.4426950408889634f;
-    bwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p, scale_log2);
-    *nlaunch += 1;
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  const int64_t qrows = (int64_t)a.n * a.h * a.lq;
-  if (qrows > 0) {
-    bwd_convert_dq_kernel<<<(unsigned)((qrows + 7) / 8), 256, 0, s>>>(p);
-    *nlaunch += 1;
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  if (blocks == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // The register split is only sound at exactly kRegsLaunch registers per
+  // thread; refuse to launch otherwise (setmaxnreg.inc would never return).
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  const float scale_log2 = a.scale * 1.4426950408889634f;
+  bwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p, scale_log2);
+  *nlaunch += 1;
+  return cudaGetLastError();
 }
 
 }  // namespace
 
+cudaError_t launch_bwd_prepare(const BwdParams& p, cudaStream_t s, int* nlaunch) {
+  const int64_t rows = (int64_t)p.a.n * p.a.h * p.lq_pad;
+  if (rows == 0) return cudaSuccess;
+  bwd_preprocess_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+  *nlaunch += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
+  if (p.a.d == 128) return launch_bwd_main_d<128>(p, tq, tk, tv, tdo, s, nlaunch);
+  if (p.a.d == 64) return launch_bwd_main_d<64>(p, tq, tk, tv, tdo, s, nlaunch);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch) {
+  const int64_t qrows = (int64_t)p.a.n * p.a.h * p.a.lq;
+  if (qrows == 0) return cudaSuccess;
+  bwd_convert_dq_kernel<<<(unsigned)((qrows + 7) / 8), 256, 0, s>>>(p);
+  *nlaunch += 1;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_bf16(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
-  if (p.a.d == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, s, nlaunch);
-  if (p.a.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, s, nlaunch);
-  return cudaErrorInvalidValue;
+  if (p.a.d != 64 && p.a.d != 128) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = launch_bwd_prepare(p, s, nlaunch)) != cudaSuccess) return e;
+  if ((e = launch_bwd_main(p, tq, tk, tv, tdo, s, nlaunch)) != cudaSuccess) return e;
+  return launch_bwd_finish(p, s, nlaunch);
 }
 
 }  // namespace bea

@@ -85,8 +85,16 @@ struct BwdParams {
   uint32_t* status;
 };
 // Tensor maps over q, k, v, dout are built by the caller (api.cu).
+// launch_bwd_bf16 = prepare (D, lse*log2e, zeroed dQ accumulator) + main
+// (dK, dV, dQ accumulation) + finish (dQ = scale * accumulator); the stages
+// are also exported separately for callers that accumulate dQ over several
+// K/V blocks.
 cudaError_t launch_bwd_bf16(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s, int* nlaunch);
+cudaError_t launch_bwd_prepare(const BwdParams& p, cudaStream_t s, int* nlaunch);
+cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s, int* nlaunch);
+cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch);
 
 cudaError_t launch_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 

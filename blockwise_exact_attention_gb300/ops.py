@@ -104,6 +104,51 @@ def flash_mha_bwd(dout, q, k, v, out, lse, softmax_scale=None, is_causal=False, 
     return dq, dk, dv
 
 
+def _ws_args(workspace, q_like):
+    if workspace is None:
+        raise ValueError("the staged backward needs the caller's workspace (bwd_workspace_bytes)")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def flash_mha_bwd_prepare(dout, out, lse, workspace):
+    """Stage 1 of the staged backward: D, lse*log2(e) and a zeroed fp32 dQ
+    accumulator in ``workspace`` (bf16 inputs)."""
+    lib = _lib.load()
+    ds = [_desc(x) for x in (dout, out, lse)]
+    wp, wb = _ws_args(workspace, dout)
+    rc = lib.bea_flash_mha_bwd_prepare(*[_ref(x) for x in ds], wp, wb, _stream())
+    _lib.check(rc, "flash_mha_bwd_prepare")
+    _count()
+
+
+def flash_mha_bwd_kv_block(dout, q, k, v, dk, dv, softmax_scale=None, is_causal=False, window_size=(-1, -1),
+                           accumulate=False, workspace=None):
+    """Stage 2: one K/V block's dK, dV (written or added) and its share of dQ
+    (added into the workspace accumulator)."""
+    lib = _lib.load()
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[3])
+    ds = [_desc(x) for x in (dout, q, k, v, dk, dv)]
+    wp, wb = _ws_args(workspace, q)
+    rc = lib.bea_flash_mha_bwd_kv_block(*[_ref(x) for x in ds], float(softmax_scale), int(bool(is_causal)),
+                                        int(window_size[0]), int(window_size[1]), int(bool(accumulate)), wp, wb,
+                                        _stream())
+    _lib.check(rc, "flash_mha_bwd_kv_block")
+    _count()
+    return dk, dv
+
+
+def flash_mha_bwd_finish(dq, softmax_scale, accumulate=False, workspace=None):
+    """Stage 3: dq = softmax_scale * accumulator (written, or added to an fp32 dq)."""
+    lib = _lib.load()
+    wp, wb = _ws_args(workspace, dq)
+    rc = lib.bea_flash_mha_bwd_finish(_ref(_desc(dq)), float(softmax_scale), int(bool(accumulate)), wp, wb,
+                                      _stream())
+    _lib.check(rc, "flash_mha_bwd_finish")
+    _count()
+    return dq
+
+
 def flash_mha_bwd_noalloc(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale=None, is_causal=False,
                           window_size=(-1, -1), accumulate=False):
     """flash_mha_bwd for callers that cannot allocate: the workspace is the

@@ -11,7 +11,10 @@ flash_sharding.py, sections "Ring Forward" and "Ring Backward").
 On one GPU the K/V "rotation" is a zero-copy chunk view of the resident
 tensors, so the schedule reduces to a sequence of forward calls and merges,
 all through the C ABI. The backward runs every visible chunk pair once with
-the final out/lse of its query rows and adds the partial gradients in fp32.
+the final out/lse of its query rows and adds the partial gradients in fp32;
+for bf16 inputs it uses the staged backward, so that D is computed once per
+query chunk and dQ stays in the fp32 workspace accumulator across its K/V
+chunks.
 """
 
 from __future__ import annotations
@@ -107,13 +110,23 @@ def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=Non
     qs, ks, vs = _chunks(q, n_chunks, 1), _chunks(k, n_chunks, 1), _chunks(v, n_chunks, 1)
     dos, os_, ls = _chunks(dout, n_chunks, 1), _chunks(out, n_chunks, 1), _chunks(lse, n_chunks, 2)
     dqs, dks, dvs = _chunks(dq, n_chunks, 1), _chunks(dk, n_chunks, 1), _chunks(dv, n_chunks, 1)
+    staged = q.dtype == torch.bfloat16
     for i, steps in enumerate(chunk_schedule(n_chunks, is_causal)):
-        for _t, j, kind in steps:
-            if kind == "skip":
-                continue
+        live = [(j, kind) for _t, j, kind in steps if kind != "skip"]
+        if staged:
+            # D of query chunk i once, its dQ summed over every visible K/V chunk in the fp32
+            # workspace accumulator, one conversion at the end
+            ops.flash_mha_bwd_prepare(dos[i], os_[i], ls[i], ws)
+        for j, kind in live:
             # causal, query chunks in ascending order: the diagonal pair (i, i) is the
-            # first to touch dq_i, dk_i and dv_i, so it overwrites instead of adding
+            # first to touch dk_i and dv_i, so it overwrites instead of adding
             first = is_causal and kind == "causal"
-            ops.flash_mha_bwd(dos[i], qs[i], ks[j], vs[j], os_[i], ls[i], softmax_scale, kind == "causal",
-                              dq=dqs[i], dk=dks[j], dv=dvs[j], accumulate=not first, workspace=ws)
+            if staged:
+                ops.flash_mha_bwd_kv_block(dos[i], qs[i], ks[j], vs[j], dks[j], dvs[j], softmax_scale,
+                                           kind == "causal", accumulate=not first, workspace=ws)
+            else:
+                ops.flash_mha_bwd(dos[i], qs[i], ks[j], vs[j], os_[i], ls[i], softmax_scale, kind == "causal",
+                                  dq=dqs[i], dk=dks[j], dv=dvs[j], accumulate=not first, workspace=ws)
+        if staged:
+            ops.flash_mha_bwd_finish(dqs[i], softmax_scale, accumulate=False, workspace=ws)
     return dq, dk, dv

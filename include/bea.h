@@ -139,6 +139,43 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
                       void* stream);
 
 /*
+ * The bf16 backward in its three stages, for a caller that accumulates the dQ
+ * of one set of query rows over several K/V blocks: the backward of ring
+ * attention, where each query chunk meets every visible K/V chunk once
+ * (flash_attn_jax flash_sharding.py, "Ring Backward": dq accumulates over the
+ * steps; picotron context_parallel.py, RingAttentionFunc.backward). Running
+ * prepare once, kv_block once per K/V block, then finish once keeps dQ in
+ * fp32 in the workspace across blocks and computes D once per query chunk.
+ * bea_flash_mha_bwd on bf16 inputs is exactly prepare + kv_block + finish.
+ *
+ * All three take the same workspace, sized by
+ * bea_flash_mha_bwd_workspace_size(n, lq, h, d) of the query-side tensors,
+ * 256-byte aligned. Between prepare and finish it holds the state of the
+ * accumulation; calls on it must be ordered on one stream. Only bf16 q/k/v
+ * are supported (f32 inputs: BEA_ERR_UNSUPPORTED; use bea_flash_mha_bwd).
+ *
+ * prepare  (Step "D = rowsum(dO * O)"): dout [n, lq, h, d] bf16;
+ *          out same shape, bf16 or f32; lse [n, h, lq] f32. Writes D and
+ *          lse * log2(e) per row and zeroes the fp32 dQ accumulator.
+ * kv_block (Steps P, dV, dP, dS, dK, and dQ's sum over these keys): dout,
+ *          q [n, lq, h, d] bf16, k, v [n, lk, h_kv, d] bf16; dk, dv
+ *          [n, lk, h_kv, d] bf16 or f32, written (accumulate 0) or added to
+ *          (accumulate 1, both f32). Adds this block's dS k into the
+ *          accumulator. The mask arguments are those of bea_flash_mha_bwd and
+ *          apply to this (q, k) pair.
+ * finish   dq [n, lq, h, d] bf16 or f32: dq = softmax_scale * accumulator,
+ *          written (accumulate 0) or added to an f32 dq (accumulate 1).
+ */
+int bea_flash_mha_bwd_prepare(const bea_tensor* dout, const bea_tensor* out, const bea_tensor* lse,
+                              void* workspace, size_t workspace_bytes, void* stream);
+int bea_flash_mha_bwd_kv_block(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k,
+                               const bea_tensor* v, const bea_tensor* dk, const bea_tensor* dv,
+                               float softmax_scale, int is_causal, int window_left, int window_right,
+                               int accumulate, void* workspace, size_t workspace_bytes, void* stream);
+int bea_flash_mha_bwd_finish(const bea_tensor* dq, float softmax_scale, int accumulate, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * bea_flash_mha_bwd without a caller-supplied workspace. (The pages have no
  * counterpart; this is a library convenience.)
  *

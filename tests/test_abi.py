@@ -134,6 +134,40 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call(out=T([1, 256, 4, 128], F32), ws=FAKE + 8) == WS
 
 
+def test_staged_bwd_rejects_bad_arguments(lib):
+    q, k, v, o, l = good()
+    do = T([1, 256, 4, 128])
+    dq, dk, dv = T([1, 256, 4, 128], F32), T([1, 256, 2, 128], F32), T([1, 256, 2, 128], F32)
+    need = lib.bea_flash_mha_bwd_workspace_size(1, 256, 4, 128)
+    r = ctypes.byref
+
+    def prep(do=do, out=o, lse=l, ws=FAKE, wsb=need):
+        return lib.bea_flash_mha_bwd_prepare(r(do), r(out), r(lse), ws, wsb, None)
+
+    def block(q=q, k=k, dk=dk, dv=dv, acc=1, ws=FAKE, wsb=need, causal=1, wr=-1):
+        return lib.bea_flash_mha_bwd_kv_block(r(do), r(q), r(k), r(v), r(dk), r(dv), 0.125, causal, -1, wr, acc,
+                                              ws, wsb, None)
+
+    def fin(dq=dq, acc=0, ws=FAKE, wsb=need, scale=0.125):
+        return lib.bea_flash_mha_bwd_finish(r(dq), scale, acc, ws, wsb, None)
+
+    assert prep(wsb=need - 1) == WS
+    assert prep(ws=FAKE + 64) == WS
+    assert prep(lse=T([1, 4, 255], F32)) == SHAPE
+    assert prep(do=T([1, 256, 4, 128], F32), out=T([1, 256, 4, 128], F32)) == UNSUP
+    assert prep(do=T([1, 256, 4, 96]), out=T([1, 256, 4, 96])) == UNSUP
+    assert block(wsb=need - 1) == WS
+    assert block(dk=T([1, 256, 2, 128], BF16)) == DTYPE        # accumulate needs f32
+    assert block(dk=T([1, 256, 4, 128], F32)) == SHAPE
+    assert block(acc=2) == ARG
+    assert block(wr=3) == ARG                                  # causal with a right window
+    assert block(q=T([1, 256, 4, 128], F32), k=T([1, 256, 2, 128], F32)) == DTYPE
+    assert fin(acc=1, dq=T([1, 256, 4, 128], BF16)) == DTYPE
+    assert fin(scale=0.0) == ARG
+    assert fin(wsb=need - 1) == WS
+    assert fin(dq=T([1, 256, 4, 64], F32), wsb=lib.bea_flash_mha_bwd_workspace_size(1, 256, 4, 64) - 1) == WS
+
+
 def test_merge_rejects_bad_arguments(lib):
     r = ctypes.byref
     acc, la = T([1, 64, 2, 128], F32), T([1, 2, 64], F32)

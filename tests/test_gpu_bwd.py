@@ -166,3 +166,52 @@ def test_bwd_full_size_head_subset(name):
     others = [hh for hh in range(w.h) if hh not in hqs]
     if others:
         assert float(dq[:, :, others].abs().max()) == 0.0
+
+
+# ---- the staged backward (prepare / kv_block / finish) -------------------------------------
+
+def test_staged_bwd_equals_one_call():
+    """prepare + kv_block + finish launch the same kernels as flash_mha_bwd."""
+    import blockwise_exact_attention_gb300 as bea
+    x = workloads.small_case(n=1, l=515, h=4, h_kv=2, d=128, seed=31)
+    scale = 1.0 / math.sqrt(128)
+    out_up, lse_up = _bwd_inputs(x, scale, True, (-1, -1))
+    q, k, v, do = (to_dev(x[s], torch.bfloat16) for s in ("q", "k", "v", "dout"))
+    o, lse = to_dev(out_up, torch.bfloat16), to_dev(lse_up, torch.float32)
+    ref = bea.flash_mha_bwd(do, q, k, v, o, lse, scale, True, grad_dtype=torch.float32)
+    ws = torch.empty(bea.bwd_workspace_bytes(q), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = (torch.empty_like(t) for t in ref)
+    bea.flash_mha_bwd_prepare(do, o, lse, ws)
+    bea.flash_mha_bwd_kv_block(do, q, k, v, dk, dv, scale, True, workspace=ws)
+    bea.flash_mha_bwd_finish(dq, scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert torch.allclose(dq, ref[0], atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_staged_bwd_accumulates_dq_over_kv_blocks(d):
+    """Keys split into two blocks: dQ summed in the workspace over both, dK/dV per block,
+    against the oracle backward over all keys."""
+    import blockwise_exact_attention_gb300 as bea
+    lq, lk = 300, 520
+    x = workloads.small_case(n=1, l=lq, h=4, h_kv=2, d=d, seed=32 + d, lk=lk)
+    scale = 1.0 / math.sqrt(d)
+    out_up, lse_up = _bwd_inputs(x, scale, False, (-1, -1))
+    q, k, v, do = (to_dev(x[s], torch.bfloat16) for s in ("q", "k", "v", "dout"))
+    o, lse = to_dev(out_up, torch.bfloat16), to_dev(lse_up, torch.float32)
+    ws = torch.empty(bea.bwd_workspace_bytes(q), dtype=torch.uint8, device="cuda")
+    dq = torch.full(q.shape, 7.0, device="cuda")  # overwritten by finish
+    dk = torch.empty(k.shape, device="cuda")
+    dv = torch.empty(v.shape, device="cuda")
+    cut = 256  # a 16-byte aligned chunk view boundary
+    bea.flash_mha_bwd_prepare(do, o, lse, ws)
+    for sl in (slice(0, cut), slice(cut, lk)):
+        bea.flash_mha_bwd_kv_block(do, q, k[:, sl], v[:, sl], dk[:, sl], dv[:, sl], scale, False, workspace=ws)
+    bea.flash_mha_bwd_finish(dq, scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    rdq, rdk, rdv = oracle.attention_bwd(x["dout"], x["q"], x["k"], x["v"], out_up, lse_up, scale, False)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), (rdq, rdk, rdv)):
+        assert_close_bf16(to_np(g), r, name, output_is_bf16=False)
