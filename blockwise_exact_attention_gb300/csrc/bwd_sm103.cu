@@ -16,9 +16,9 @@
 //      shared memory; the CTA walks the group's query heads x the 128-row
 //      query tiles the causal/window band lets it see, each tile as two
 //      64-query halves:
-//        warp 8      producer: K, V once; per tile Q_i and dO_i (TMA) and the
+//        warp 12     producer: K, V once; per tile Q_i and dO_i (TMA) and the
 //                    tile's L2 and D rows (bulk copies) into 2 stages,
-//        warp 9      MMA issuer (the whole warp, one elected lane issues):
+//        warp 13     MMA issuer (the whole warp, one elected lane issues):
 //                    per half h, S_h^T = K Q_h^T and dP_h^T = V dO_h^T into
 //                    TMEM slot h; then, per half as soon as its P^T / dS^T
 //                    are ready, dV += P_h^T dO_h (P^T from TMEM),
@@ -27,9 +27,11 @@
 //                    are issued ahead of this tile's second-half gradient
 //                    products, so the key warps never wait for a whole tile
 //                    of tensor work,
-//        warps 0-3   one thread per key: P^T and dS^T of one half from S^T,
-//                    dP^T, L2, D; finally the dK/dV epilogue,
-//        warps 4-7   one thread per head-dim index: read dQ_h^T out of TMEM
+//        warps 0-7   two warpgroups, one thread per key each: warpgroup c
+//                    forms P^T and dS^T of queries [32c, 32c+32) of every
+//                    half from S^T, dP^T, L2, D; finally warpgroup 0 writes
+//                    dV and warpgroup 1 dK,
+//        warps 8-11  one thread per head-dim index: read dQ_h^T out of TMEM
 //                    and add it into the fp32 accumulator; the 32 lanes of a
 //                    warp cover 32 consecutive entries of a query row, so each
 //                    reduction instruction is one contiguous 128-byte line.
@@ -52,18 +54,19 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per iteration
 constexpr int kBN = 128;  // keys per CTA
-constexpr int kThreads = 384;  // 3 warpgroups
-// Register split: launched at kRegsLaunch per thread (65536 / 384 rounded
-// down to 8); the key-row warpgroup rises to kRegsCompute, the dQ drain and
-// the producer/MMA warpgroup drop to kRegsDrain and kRegsOther:
-// 128 * (224 + 128 + 152) = 384 * 168.
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsCompute = 224;
-constexpr int kRegsDrain = 128;
-constexpr int kRegsOther = 152;
-static_assert(kRegsCompute + kRegsDrain + kRegsOther == 3 * kRegsLaunch, "register split");
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 512;  // 4 warpgroups
+// Register split: launched at kRegsLaunch per thread (65536 / 512); the two
+// key-row warpgroups rise to kRegsCompute, the dQ drain and the producer/MMA
+// warpgroup drop to kRegsDrain and kRegsOther:
+// 128 * (2 * 152 + 80 + 128) = 512 * 128.
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsCompute = 152;
+constexpr int kRegsDrain = 80;
+constexpr int kRegsOther = 128;
+static_assert(2 * kRegsCompute + kRegsDrain + kRegsOther == 4 * kRegsLaunch, "register split");
+constexpr int kDrainWarp0 = 8;  // warps 8-11
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 
 template <int D>
 struct BwdCfg {
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&do_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
-      mbar_init(&ready[s], 128);
+      mbar_init(&ready[s], 256);
       mbar_init(&sp_full[s], 1);
       mbar_init(&dq_full[s], 1);
       mbar_init(&dq_empty[s], 128);
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM slot h: S_h^T at 128h (P_h^T over its first 32 columns), dP_h^T / dQ_h^T at 128h + 64
   const uint32_t T_DP = 64, T_DV = 256, T_DK = 384;
 
-  if (warp >= 8) {
+  if (warp >= kProducerWarp) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
   if (warp == kProducerWarp) {
     // ========================== TMA producer ==========================
@@ -476,12 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   }
-  } else if (warp < 4) {
+  } else if (warp < kDrainWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
     // ========================== P^T / dS^T (one thread per key) ==========================
-    const int j = threadIdx.x;  // key row == TMEM lane
+    // Key warpgroup c (warps 4c..4c+3) takes queries [32c, 32c+32) of every half.
+    const int c = warp / 4;
+    const int j = threadIdx.x % 128;  // key row == TMEM lane
     const int kj = sc.k0 + j;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
     uint8_t* ds_row = smem + C::kDSOff + j * 128;
     bool ok = true;
     for (int it = 0; ok && it < sc.n_iter; ++it) {
@@ -497,85 +502,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait_parity(&sp_full[h], it & 1, abort_flag, p.status))) break;
         tc_fence_after();
         const uint32_t slot = tmem + lane_base + 128u * h;
-        uint32_t sv0[32], pv0[32], sv1[32], pv1[32];
-        tmem_ld32(slot, sv0);
-        tmem_ld32(slot + T_DP, pv0);
+        uint32_t sv[32], pv[32];
+        tmem_ld32(slot + 32 * c, sv);
+        tmem_ld32(slot + T_DP + 32 * c, pv);
         tmem_wait_ld();
-        reg_fence<32>(sv0);
-        reg_fence<32>(pv0);
-        tmem_ld32(slot + 32, sv1);  // in flight while chunk 2h is processed
-        tmem_ld32(slot + T_DP + 32, pv1);
+        reg_fence<32>(sv);
+        reg_fence<32>(pv);
         if (need_mask)
-          bwd_chunk<D, true>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, slot, ds_row, j);
+          bwd_chunk<D, true>(sv, pv, l2s, dds, 2 * h + c, a, kj, q0, scale_log2, slot + 16 * c, ds_row, j);
         else
-          bwd_chunk<D, false>(sv0, pv0, l2s, dds, 2 * h, a, kj, q0, scale_log2, slot, ds_row, j);
-        tmem_wait_ld();
-        reg_fence<32>(sv1);
-        reg_fence<32>(pv1);
-        if (need_mask)
-          bwd_chunk<D, true>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, slot + 16, ds_row, j);
-        else
-          bwd_chunk<D, false>(sv1, pv1, l2s, dds, 2 * h + 1, a, kj, q0, scale_log2, slot + 16, ds_row, j);
+          bwd_chunk<D, false>(sv, pv, l2s, dds, 2 * h + c, a, kj, q0, scale_log2, slot + 16 * c, ds_row, j);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
         mbar_arrive(&ready[h]);
       }
     }
-    // ---- dK / dV epilogue ----
+    // ---- dK / dV epilogue: key warpgroup 0 writes dV, warpgroup 1 writes dK ----
     if (ok && sc.n_iter > 0) ok = warp_wait_parity(dkv_full, 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const bool have = sc.n_iter > 0;
+      const float mul = c ? a.scale : 1.f;
+      const bool f32 = c ? p.dk_is_f32 : p.dv_is_f32;
+      const int64_t off0 = c ? (b * p.dk.sn + (int64_t)kj * p.dk.sl + kvh * p.dk.sh)
+                             : (b * p.dv.sn + (int64_t)kj * p.dv.sl + kvh * p.dv.sh);
+      void* base = c ? p.dk.ptr : p.dv.ptr;
+      const uint32_t src_t = tmem + lane_base + (c ? T_DK : T_DV);
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t vv[32], kk[32];
+        uint32_t src[32];
         if (have) {
-          tmem_ld32(tmem + lane_base + T_DV + c0, vv);
-          tmem_ld32(tmem + lane_base + T_DK + c0, kk);
+          tmem_ld32(src_t + c0, src);
           tmem_wait_ld();
-          reg_fence<32>(vv);
-          reg_fence<32>(kk);
+          reg_fence<32>(src);
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) vv[c] = kk[c] = 0u;
+          for (int e = 0; e < 32; ++e) src[e] = 0u;
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) kk[c] = __float_as_uint(__uint_as_float(kk[c]) * a.scale);
+        for (int e = 0; e < 32; ++e) src[e] = __float_as_uint(__uint_as_float(src[e]) * mul);
         if (kj >= a.lk) continue;  // ragged last key block: the loads above stay warp-wide
+        if (f32) {
+          float* dst = reinterpret_cast<float*>(base) + off0 + c0;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t* src = which ? kk : vv;
-          const bool f32 = which ? p.dk_is_f32 : p.dv_is_f32;
-          void* base = which ? p.dk.ptr : p.dv.ptr;
-          const int64_t off = which ? (b * p.dk.sn + (int64_t)kj * p.dk.sl + kvh * p.dk.sh + c0)
-                                    : (b * p.dv.sn + (int64_t)kj * p.dv.sl + kvh * p.dv.sh + c0);
-          if (f32) {
-            float* dst = reinterpret_cast<float*>(base) + off;
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              float4 v4 = make_float4(__uint_as_float(src[c]), __uint_as_float(src[c + 1]),
-                                      __uint_as_float(src[c + 2]), __uint_as_float(src[c + 3]));
-              if (p.accumulate) {
-                const float4 o = *reinterpret_cast<const float4*>(dst + c);
-                v4.x += o.x;
-                v4.y += o.y;
-                v4.z += o.z;
-                v4.w += o.w;
-              }
-              *reinterpret_cast<float4*>(dst + c) = v4;
+          for (int e = 0; e < 32; e += 4) {
+            float4 v4 = make_float4(__uint_as_float(src[e]), __uint_as_float(src[e + 1]),
+                                    __uint_as_float(src[e + 2]), __uint_as_float(src[e + 3]));
+            if (p.accumulate) {
+              const float4 o = *reinterpret_cast<const float4*>(dst + e);
+              v4.x += o.x;
+              v4.y += o.y;
+              v4.z += o.z;
+              v4.w += o.w;
             }
-          } else {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + off;
+            *reinterpret_cast<float4*>(dst + e) = v4;
+          }
+        } else {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + off0 + c0;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 v4;
-              v4.x = pack_bf16x2(__uint_as_float(src[c]), __uint_as_float(src[c + 1]));
-              v4.y = pack_bf16x2(__uint_as_float(src[c + 2]), __uint_as_float(src[c + 3]));
-              v4.z = pack_bf16x2(__uint_as_float(src[c + 4]), __uint_as_float(src[c + 5]));
-              v4.w = pack_bf16x2(__uint_as_float(src[c + 6]), __uint_as_float(src[c + 7]));
-              *reinterpret_cast<uint4*>(dst + c) = v4;
-            }
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v4;
+            v4.x = pack_bf16x2(__uint_as_float(src[e]), __uint_as_float(src[e + 1]));
+            v4.y = pack_bf16x2(__uint_as_float(src[e + 2]), __uint_as_float(src[e + 3]));
+            v4.z = pack_bf16x2(__uint_as_float(src[e + 4]), __uint_as_float(src[e + 5]));
+            v4.w = pack_bf16x2(__uint_as_float(src[e + 6]), __uint_as_float(src[e + 7]));
+            *reinterpret_cast<uint4*>(dst + e) = v4;
           }
         }
       }
@@ -584,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(kRegsDrain <= kRegsLaunch, "the drain warpgroup gives registers back");
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDrain));
     // ========================== dQ drain (one thread per head-dim index) ==========================
-    const int dd = threadIdx.x - 128;  // dQ^T row == head-dim index == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const int dd = threadIdx.x - 32 * kDrainWarp0;  // dQ^T row == head-dim index == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
     const bool live = dd < D;  // for d = 64 the upper 64 lanes hold padding rows
     bool ok = true;
     for (int it = 0; ok && it < sc.n_iter; ++it) {
