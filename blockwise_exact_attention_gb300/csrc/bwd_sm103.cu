@@ -23,10 +23,10 @@
 //                    TMEM slot h; then, per half as soon as its P^T / dS^T
 //                    are ready, dV += P_h^T dO_h (P^T from TMEM),
 //                    dK += dS_h^T Q_h and dQ_h^T = K^T dS_h^T (dS^T from
-//                    shared memory). The next tile's first-half S^T / dP^T
-//                    are issued ahead of this tile's second-half gradient
-//                    products, so the key warps never wait for a whole tile
-//                    of tensor work,
+//                    shared memory). Each half's products for this tile are
+//                    followed at once by that half's S^T / dP^T for the
+//                    next tile, so the key warps' work on one half hides
+//                    behind the tensor work of the other,
 //        warps 0-7   two warpgroups, one thread per key each: warpgroup c
 //                    forms P^T and dS^T of queries [32c, 32c+32) of every
 //                    half from S^T, dP^T, L2, D; finally warpgroup 0 writes
@@ -425,9 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        C::kIdescQ, k > 0 ? 1u : 0u);
       };
       // Issue order: S_0 dP_0 S_1 dP_1 (tile 0), then per tile i
-      //   [P_0/dS_0 ready] grads_0(i)
-      //   [P_1/dS_1 ready] S_0 dP_0 (tile i+1), grads_1(i), S_1 dP_1 (tile i+1)
-      // so that the key warps can start on tile i+1 while the tensor core finishes tile i.
+      //   [P_0/dS_0 ready] grads_0(i), S_0 dP_0 (tile i+1)
+      //   [P_1/dS_1 ready] grads_1(i), S_1 dP_1 (tile i+1)
+      // Slot 0 is free for tile i+1 once grads_0(i) is issued and its dQ_0^T drained, so the
+      // key warps' work on each half hides behind the tensor work of the other half.
       bool ok = sc.n_iter > 0 && warp_wait_parity(kv_full, 0, abort_flag, p.status);
       if (ok) ok = warp_wait_parity(&q_full[0], 0, abort_flag, p.status);
       if (ok) ok = warp_wait_parity(&do_full[0], 0, abort_flag, p.status);
@@ -444,32 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it & 1, s1 = s ^ 1;
         const uint32_t par1 = ((it + 1) >> 1) & 1;
         const bool more = it + 1 < sc.n_iter;
-        if (!(ok = warp_wait_parity(&ready[0], it & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_grads(0, s, it == 0);
-        umma_commit_warp(&dq_full[0]);
-        if (!(ok = warp_wait_parity(&ready[1], it & 1, abort_flag, p.status))) break;
-        if (more) {
-          if (!(ok = warp_wait_parity(&q_full[s1], par1, abort_flag, p.status))) break;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = warp_wait_parity(&ready[h], it & 1, abort_flag, p.status))) break;
           tc_fence_after();
-          issue_s(0, s1);
-          // dQ_0^T of tile i occupies the dP_0^T columns until the drain has read it
-          if (!(ok = warp_wait_parity(&dq_empty[0], it & 1, abort_flag, p.status))) break;
-          if (!(ok = warp_wait_parity(&do_full[s1], par1, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_dp(0, s1);
-          umma_commit_warp(&sp_full[0]);
-        }
-        tc_fence_after();
-        issue_grads(1, s, false);
-        umma_commit_warp(&dq_full[1]);
-        umma_commit_warp(&qdo_empty[s]);  // the last readers of stage s are issued
-        if (more) {
-          issue_s(1, s1);
-          if (!(ok = warp_wait_parity(&dq_empty[1], it & 1, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_dp(1, s1);
-          umma_commit_warp(&sp_full[1]);
+          issue_grads(h, s, it == 0 && h == 0);
+          umma_commit_warp(&dq_full[h]);
+          if (h == 1) umma_commit_warp(&qdo_empty[s]);  // the last readers of stage s are issued
+          if (more) {
+            if (h == 0 && !(ok = warp_wait_parity(&q_full[s1], par1, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_s(h, s1);
+            // dQ_h^T of tile i occupies the dP_h^T columns until the drain has read it
+            if (!(ok = warp_wait_parity(&dq_empty[h], it & 1, abort_flag, p.status))) break;
+            if (h == 0 && !(ok = warp_wait_parity(&do_full[s1], par1, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_dp(h, s1);
+            umma_commit_warp(&sp_full[h]);
+          }
         }
       }
       if (ok && sc.n_iter > 0) umma_commit_warp(dkv_full);
