@@ -21,8 +21,8 @@
 //        warp 13     MMA issuer (the whole warp, one elected lane issues):
 //                    per half h, S_h^T = K Q_h^T and dP_h^T = V dO_h^T into
 //                    TMEM slot h; then, per half as soon as its P^T / dS^T
-//                    are ready, dV += P_h^T dO_h (P^T from TMEM),
-//                    dK += dS_h^T Q_h and dQ_h^T = K^T dS_h^T (dS^T from
+//                    are ready, dV += P_h^T dO_h and dK += dS_h^T Q_h (P^T,
+//                    dS^T from TMEM) and dQ_h^T = K^T dS_h^T (dS^T from
 //                    shared memory). Each half's products for this tile are
 //                    followed at once by that half's S^T / dP^T for the
 //                    next tile, so the key warps' work on one half hides
@@ -42,8 +42,10 @@
 //   3. convert: dQ = scale * accumulator, cast or added into the caller's dq.
 //
 // TMEM (512 columns): slot h = [128h, 128h+128) holds S_h^T in its first 64
-// columns (P_h^T packed bf16 over the first 32 of them) and dP_h^T in the
-// last 64 (later dQ_h^T); dV [256,256+D), dK [384,384+D).
+// columns and dP_h^T in the last 64 (later dQ_h^T); dV [256,256+D), dK
+// [384,384+D). Key warpgroup c overwrites the 32 S^T columns it has read,
+// [128h + 32c, +32), with its queries' P^T (16 columns of packed bf16 pairs)
+// and dS^T (16 columns): the TMEM A operands of dV += P^T dO and dK += dS^T Q.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -237,8 +239,10 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv
     dk[e4 * 2] = pack_bf16x2(dsr[0], dsr[1]);
     dk[e4 * 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
   }
-  // P^T (packed bf16 pairs) over S^T columns that this thread has already read
+  // P^T and dS^T (packed bf16 pairs) over the 32 S^T columns this thread has just read:
+  // P^T in the first 16, dS^T in the last 16 (the A operands of dV += P^T dO and dK += dS^T Q)
   tmem_st16(p_dst, pk);
+  tmem_st16(p_dst + 16, dk);
   // dS^T row j, queries [32cc, 32cc+32): 4 chunks of 16 B, 128-byte swizzle
   uint8_t* half = ds_row + (cc >> 1) * 16384;
 #pragma unroll
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM slot h: S_h^T at 128h (P_h^T over its first 32 columns), dP_h^T / dQ_h^T at 128h + 64
+  // TMEM slot h: S_h^T at 128h (then P^T / dS^T, 16 + 16 columns per key warpgroup), dP_h^T / dQ_h^T at 128h + 64
   const uint32_t T_DP = 64, T_DV = 256, T_DK = 384;
 
   if (warp >= kProducerWarp) {
@@ -377,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
       const uint64_t k_mn = sdesc_sw128(smem_u32(smem + C::kKOff), 16384, 1024);
       const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + C::kVOff), 16, 1024);
-      const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + C::kDSOff), 16, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + C::kDSOff), 16384, 1024);
       const uint64_t q_kmaj0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
       const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16384, 1024);
@@ -405,20 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                        k > 0 ? 1u : 0u);
         }
       };
-      // dV += P_h^T dO_h (A = P_h^T from TMEM, B = dO MN-major); dK += dS_h^T Q_h (A = dS^T
-      // K-major, B = Q MN-major); dQ_h^T = K^T dS_h^T (A = K read MN-major, B = dS_h^T
-      // MN-major) into the second half of slot h
+      // dV += P_h^T dO_h (A = P_h^T from TMEM, B = dO MN-major); dK += dS_h^T Q_h (A = dS_h^T
+      // from TMEM, B = Q MN-major); dQ_h^T = K^T dS_h^T (A = K read MN-major, B = dS_h^T from
+      // shared memory, MN-major) into the second half of slot h. Query step k (16 queries)
+      // of the half was formed by key warpgroup k / 2, whose P^T / dS^T columns are
+      // [128h + 32 (k / 2), +16) / [128h + 32 (k / 2) + 16, +16).
       auto issue_grads = [&](int h, int st, bool first) {
         const uint64_t q_mn = sdesc_add(q_mn0, st * C::kTileBytes);
         const uint64_t do_mn = sdesc_add(do_mn0, st * C::kTileBytes);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ts_warp(tmem + T_DV, tmem + 128u * h + k * 8, sdesc_add(do_mn, (4 * h + k) * 2048), C::kIdescKV,
-                       (!first || k > 0) ? 1u : 0u);
+          umma_ts_warp(tmem + T_DV, tmem + 128u * h + 32 * (k / 2) + 8 * (k % 2), sdesc_add(do_mn, (4 * h + k) * 2048),
+                       C::kIdescKV, (!first || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss_warp(tmem + T_DK, sdesc_add(ds_kmaj, h * 16384 + k * 32), sdesc_add(q_mn, (4 * h + k) * 2048),
-                       C::kIdescKV, (!first || k > 0) ? 1u : 0u);
+          umma_ts_warp(tmem + T_DK, tmem + 128u * h + 32 * (k / 2) + 16 + 8 * (k % 2),
+                       sdesc_add(q_mn, (4 * h + k) * 2048), C::kIdescKV, (!first || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
           umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048),
@@ -502,9 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<32>(sv);
         reg_fence<32>(pv);
         if (need_mask)
-          bwd_chunk<D, true>(sv, pv, l2s, dds, 2 * h + c, a, kj, q0, scale_log2, slot + 16 * c, ds_row, j);
+          bwd_chunk<D, true>(sv, pv, l2s, dds, 2 * h + c, a, kj, q0, scale_log2, slot + 32 * c, ds_row, j);
         else
-          bwd_chunk<D, false>(sv, pv, l2s, dds, 2 * h + c, a, kj, q0, scale_log2, slot + 16 * c, ds_row, j);
+          bwd_chunk<D, false>(sv, pv, l2s, dds, 2 * h + c, a, kj, q0, scale_log2, slot + 32 * c, ds_row, j);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
