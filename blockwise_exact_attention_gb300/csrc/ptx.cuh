@@ -62,6 +62,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware until it completes or `hint_ns` passes, instead of
+// returning at once. Waiting warps then stop polling the barrier through the
+// shared-memory pipe, which the tensor core's operand reads also use.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Longest single suspension inside wait_parity(); the wall-clock limit is
+// checked between suspensions.
+#ifndef BEA_WAIT_SLEEP_NS
+#define BEA_WAIT_SLEEP_NS 1000000u
+#endif
+
 // Wall-clock limit of one wait. Pipelines here never legitimately wait more
 // than microseconds; a wait this long means a lost arrive.
 #ifndef BEA_WAIT_LIMIT_NS
@@ -70,22 +92,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait until the phase with parity `parity` of `bar` has completed. Returns
 // false (and leaves `*abort` set) when the CTA is aborting or the wait ran
-// past `limit_ns`.
+// past `limit_ns`. Between checks of the limit and of the abort flag the
+// thread sleeps on the barrier (at most BEA_WAIT_SLEEP_NS at a time).
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, volatile int* abort,
                                             uint32_t* status, uint64_t limit_ns = BEA_WAIT_LIMIT_NS) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
+  const uint32_t sleep_ns = limit_ns < BEA_WAIT_SLEEP_NS ? (uint32_t)limit_ns : BEA_WAIT_SLEEP_NS;
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((++spins & 15u) == 0u) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        report_status(status, BEA_STATUS_TIMEOUT);
-        return false;
-      }
+    if (mbar_try_wait_sleep(a, parity, sleep_ns)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      report_status(status, BEA_STATUS_TIMEOUT);
+      return false;
     }
   }
 }
