@@ -117,6 +117,38 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# FLOP counting (the throughput metric's definition; no attention arithmetic)
+# ---------------------------------------------------------------------------
+
+def visible_pairs(lq: int, lk: int, is_causal: bool, window=(-1, -1)) -> float:
+    """Number of (query i, key j) pairs with key j visible to query i: j in
+    [i - left, i + right] (an unbounded side is -1; causal forces right = 0),
+    clipped to [0, lk)."""
+    import numpy as np
+    left, right = window
+    if is_causal:
+        right = 0
+    i = np.arange(lq, dtype=np.int64)
+    lo = np.zeros(lq, dtype=np.int64) if left < 0 else np.maximum(i - left, 0)
+    hi = np.full(lq, lk - 1, dtype=np.int64) if right < 0 else np.minimum(i + right, lk - 1)
+    return float(np.maximum(hi - lo + 1, 0).sum())
+
+
+def attention_flops(n, h, lq, lk, d, is_causal, window=(-1, -1)):
+    """(fwd, bwd) algorithmic FLOPs: 4 n h l^2 d forward, halved for causal
+    (l^2 / 2 pairs), 2.5x that backward; a window counts its visible pairs."""
+    left, right = window
+    if left < 0 and (right < 0 and not is_causal):
+        pairs = float(lq) * lk
+    elif is_causal and left < 0:
+        pairs = float(lq) * lk / 2.0
+    else:
+        pairs = visible_pairs(lq, lk, is_causal, window)
+    f = 4.0 * n * h * d * pairs
+    return f, 2.5 * f
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle legs (the reference arm and the cpu_baseline field)
 # ---------------------------------------------------------------------------
 
@@ -129,7 +161,7 @@ def oracle_sample_step(x, w, heads_kv):
     q, k, v, do = x["q"][:, :, hqs], x["k"][:, :, heads_kv], x["v"][:, :, heads_kv], x["dout"][:, :, hqs]
     out, lse = oracle.attention_fwd(q, k, v, w.softmax_scale, w.is_causal, w.window)
     oracle.attention_bwd(do, q, k, v, out.astype(np.float32), lse, w.softmax_scale, w.is_causal, w.window)
-    f, b = oracle.algorithmic_flops(w.n, len(hqs), w.l, w.l, w.d, w.is_causal, w.window)
+    f, b = attention_flops(w.n, len(hqs), w.l, w.l, w.d, w.is_causal, w.window)
     return f + b
 
 
@@ -225,7 +257,6 @@ def main():
 
     import __graft_entry__ as ge
     ge.build()
-    import oracle
     import blockwise_exact_attention_gb300 as bea
     from blockwise_exact_attention_gb300 import workloads
 
@@ -246,7 +277,7 @@ def main():
 
     def flush_l2():
         flush.sum()
-    f_fwd, f_bwd = oracle.algorithmic_flops(w.n, w.h, w.l, w.l, w.d, w.is_causal, w.window)
+    f_fwd, f_bwd = attention_flops(w.n, w.h, w.l, w.l, w.d, w.is_causal, w.window)
     stream = torch.cuda.current_stream()
 
     def fwd():
@@ -366,9 +397,39 @@ def main():
     vr = torch.randn_like(qr)
     ring_ms = statistics.median(timed(lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True),
                                       5, 2))
-    rf, _ = oracle.algorithmic_flops(1, wr.h, wr.l, wr.l, wr.d, True)
+    # the unfused replay: each block written out in bf16, then ring_merge
+    ring_unfused_ms = statistics.median(timed(lambda: bea.ring_attention_fwd(
+        qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True, block_dtype=torch.bfloat16, fused=False), 5, 2))
+    rf, _ = attention_flops(1, wr.h, wr.l, wr.l, wr.d, True)
     single_ms = statistics.median(timed(lambda: bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True), 5, 2))
     del qr, kr, vr, acc, lacc, blk, lblk
+
+    # ---- the other workloads of the measurement plan: forward and backward alone ----
+    others = {}
+    for name in ("causal_mha_4k", "swa_32k_d128", "full_32k_d64"):
+        wo = workloads.WORKLOADS[name]
+        qo = torch.randn((wo.n, wo.l, wo.h, wo.d), device=dev)
+        if wo.head_scale:  # one factor U(0.5, 2) per query head, as the workload draws it
+            qo *= (0.5 + 1.5 * torch.rand((1, 1, wo.h, 1), device=dev))
+        qo = qo.to(torch.bfloat16)
+        ko = torch.randn((wo.n, wo.l, wo.h_kv, wo.d), device=dev).to(torch.bfloat16)
+        vo = torch.randn_like(ko)
+        doo = torch.randn_like(qo)
+        oo = torch.empty_like(qo)
+        lo_ = torch.empty((wo.n, wo.h, wo.l), dtype=torch.float32, device=dev)
+        dqo, dko, dvo = torch.empty_like(qo), torch.empty_like(ko), torch.empty_like(vo)
+        wso = torch.empty(bea.bwd_workspace_bytes(qo), dtype=torch.uint8, device=dev)
+        so = wo.softmax_scale
+        fo, bo = attention_flops(wo.n, wo.h, wo.l, wo.l, wo.d, wo.is_causal, wo.window)
+        tf = statistics.median(timed(lambda: bea.flash_mha_fwd(qo, ko, vo, so, wo.is_causal, wo.window, out=oo,
+                                                                lse=lo_), 3, 1))
+        tb = statistics.median(timed(lambda: bea.flash_mha_bwd(doo, qo, ko, vo, oo, lo_, so, wo.is_causal, wo.window,
+                                                                dq=dqo, dk=dko, dv=dvo, workspace=wso), 3, 1))
+        others[name] = {"workload": wo.description, "ms_fwd": tf, "ms_bwd": tb,
+                        "fwd_tflops": fo / (tf * 1e-3) / 1e12, "bwd_tflops": bo / (tb * 1e-3) / 1e12,
+                        "pct_peak_fwd": fo / (tf * 1e-3) / 1e12 / pk_burst,
+                        "pct_peak_bwd": bo / (tb * 1e-3) / 1e12 / pk_burst}
+        del qo, ko, vo, doo, oo, lo_, dqo, dko, dvo, wso
 
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
@@ -412,8 +473,12 @@ def main():
         "merge": {"kernel": "ring_merge [1,16384,16,128] f32 acc + bf16 blk", "ms": merge_ms,
                   "bytes": merge_bytes, "gbs": merge_gbs, "peak_gbs": pk_hbm, "frac": merge_gbs / pk_hbm,
                   "bound": "hbm", "traffic": NCU_TRAFFIC_BYTES["ring_merge_kernel"]},
-        "ring": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks (36 fwd + 28 merges)", "ms": ring_ms,
-                 "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms},
+        "ring": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks: the 36 chunk pairs in ring order, one "
+                             "batched call per ring step, 28 pairs as fused ring steps (merge in the forward "
+                             "epilogue); 15 launches", "ms": ring_ms,
+                 "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms,
+                 "unfused_ms": ring_unfused_ms, "unfused": "forward + ring_merge per ring step (bf16 blocks): 15 launches"},
+        "other_workloads": others,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,

@@ -7,6 +7,8 @@ Public API (all calls run in libbea.so's CUDA kernels on the current stream):
 * ``flash_mha_bwd_prepare / flash_mha_bwd_kv_block / flash_mha_bwd_finish``:
   the same backward in stages, dQ accumulated over several K/V blocks
 * ``ring_merge(out_acc, lse_acc, out_blk, lse_blk, out_final=None)``
+* ``flash_mha_fwd_merge(q, k, v, out_acc, lse_acc, ...)``: the fused ring
+  step (a block's forward folded into the accumulator)
 * ``ring_attention_fwd / ring_attention_bwd``: ring attention replayed as
   chunk steps on one GPU.
 
@@ -20,6 +22,7 @@ from .ops import (  # noqa: F401
     flash_mha_bwd_kv_block,
     flash_mha_bwd_prepare,
     flash_mha_fwd,
+    flash_mha_fwd_merge,
     launches_since_reset,
     ring_merge,
     selftest_wait_timeout,

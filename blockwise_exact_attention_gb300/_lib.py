@@ -32,6 +32,7 @@ STATUS = {
 # every symbol include/bea.h declares
 EXPORTS = (
     "bea_flash_mha_fwd",
+    "bea_flash_mha_fwd_merge",
     "bea_flash_mha_bwd_workspace_size",
     "bea_flash_mha_bwd",
     "bea_ring_merge",
@@ -79,6 +80,8 @@ def load() -> ctypes.CDLL:
     vp, i, f, sz, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_int64
     lib.bea_flash_mha_fwd.argtypes = [P, P, P, P, P, f, i, i, i, vp]
     lib.bea_flash_mha_fwd.restype = i
+    lib.bea_flash_mha_fwd_merge.argtypes = [P, P, P, P, P, P, f, i, i, i, vp]
+    lib.bea_flash_mha_fwd_merge.restype = i
     lib.bea_flash_mha_bwd_workspace_size.argtypes = [i64, i64, i64, i64]
     lib.bea_flash_mha_bwd_workspace_size.restype = sz
     lib.bea_flash_mha_bwd.argtypes = [P, P, P, P, P, P, P, P, P, f, i, i, i, i, vp, sz, vp]

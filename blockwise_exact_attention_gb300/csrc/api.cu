@@ -264,10 +264,12 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
     return finish(bea::launch_fwd_f32(p, s, &launches), launches);
   }
   bea::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
   p.a = a;
   p.out = seq4(out);
   p.out_is_f32 = out->dtype == BEA_F32;
   p.lse = lse3(lse);
+  p.merge = 0;
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
   CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
@@ -277,6 +279,43 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
     if ((rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv))) return rc;
   }
   return finish(bea::launch_fwd_bf16(p, tq, tk, tv, s, &launches), launches);
+}
+
+int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,
+                            const bea_tensor* lse_acc, const bea_tensor* out_final, float softmax_scale, int is_causal,
+                            int window_left, int window_right, void* stream) {
+  AttnDims a;
+  int rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_tensor(out_acc, 4))) return rc;
+  if (!same_shape(out_acc, q)) return BEA_ERR_SHAPE;
+  if (out_acc->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  if ((rc = check_lse(lse_acc, a))) return rc;
+  if (out_final != nullptr) {
+    if ((rc = check_tensor(out_final, 4))) return rc;
+    if (!same_shape(out_final, q)) return BEA_ERR_SHAPE;
+    if (out_final->dtype != BEA_BF16) return BEA_ERR_DTYPE;
+  }
+  if (q->dtype != BEA_BF16) return BEA_ERR_UNSUPPORTED;
+  int launches = 0;
+  if (a.n == 0 || a.h == 0 || a.lq == 0) return finish(cudaSuccess, 0);
+  bea::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.a = a;
+  p.out = seq4(out_acc);
+  p.out_is_f32 = 1;
+  p.lse = lse3(lse_acc);
+  p.merge = 1;
+  p.fin = out_final ? seq4(out_final) : Seq4{nullptr, 0, 0, 0};
+  if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  CUtensorMap tq, tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if ((rc = make_seq_map(q, &tq))) return rc;
+  if (a.lk > 0) {
+    if ((rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv))) return rc;
+  }
+  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream), &launches), launches);
 }
 
 size_t bea_flash_mha_bwd_workspace_size(int64_t n, int64_t lq, int64_t h, int64_t d) {

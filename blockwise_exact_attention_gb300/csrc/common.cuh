@@ -63,9 +63,11 @@ cudaError_t launch_bwd_f32(const F32BwdParams& p, cudaStream_t s, int* nlaunch);
 // ---- bf16 tensor-core path -------------------------------------------------------
 struct FwdParams {
   AttnDims a;
-  Seq4 out;
+  Seq4 out;  // merge: the fp32 accumulator (read and written)
   int out_is_f32;
-  Lse3 lse;
+  Lse3 lse;  // merge: the accumulator's log-sum-exp (read and written)
+  int merge;  // fold the block into (out, lse) instead of writing it
+  Seq4 fin;   // merge only: bf16 copy of the merged rows, ptr may be null
   uint32_t* status;
 };
 // Tensor maps are built by the caller (api.cu) over q, k, v.

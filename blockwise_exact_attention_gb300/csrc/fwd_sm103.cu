@@ -95,7 +95,7 @@ __device__ __forceinline__ bool tile_needs_mask(const AttnDims& a, int qs, int j
   return false;
 }
 
-template <int D>
+template <int D, bool kMerge>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const FwdParams p, float scale_log2) {
@@ -417,6 +417,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool row_ok = qi < a.lq;
       const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+      const float L = (l_sum > 0.f) ? (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f : -INFINITY;
+      float* lse_p = p.lse.ptr + b * p.lse.sn + hq * p.lse.sh + qi;
+      // Fused ring step: fold this block's (O, L) into the fp32 accumulator (out, lse) by the
+      // log-sum-exp merge of flash_attn_jax flash_sharding.py, "Ring Forward":
+      //   L' = max + log1p(exp(min - max)), acc <- acc exp(La - L') + O exp(L - L'),
+      // leaving a row whose two log-sum-exps are both -inf unchanged.
+      float wa = 0.f, wb = inv, l_new = L;
+      bool keep = false;
+      // merge: the whole accumulator row is loaded up front (its loads overlap one another
+      // instead of waiting chunk by chunk; the S registers are free by now)
+      float4 arow[kMerge ? D / 4 : 1];
+      float* acc_row = kMerge ? reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn + (int64_t)qi * p.out.sl +
+                                    hq * p.out.sh
+                              : nullptr;
+      if constexpr (kMerge) {
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c) arow[c] = *reinterpret_cast<const float4*>(acc_row + 4 * c);
+        }
+        const float la = row_ok ? *lse_p : -INFINITY;
+        const float mx = fmaxf(la, L);
+        if (mx == -INFINITY) {
+          keep = true;
+        } else {
+          const float mn = fminf(la, L);
+          l_new = mx + log1pf(expf(mn - mx));
+          wa = expf(la - l_new);
+          wb = expf(L - l_new) * inv;
+        }
+      }
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t orow[32];
@@ -428,35 +458,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) orow[c] = 0u;
         }
-        if (row_ok) {
-          if (p.out_is_f32) {
-            float* dst = reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn + (int64_t)qi * p.out.sl +
-                         hq * p.out.sh + c0;
+        if (!row_ok) continue;
+        if constexpr (kMerge) {
+          float* acc = acc_row + c0;
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const float4 v4 = make_float4(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv,
-                                            __uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
-              *reinterpret_cast<float4*>(dst + c) = v4;
+          for (int c = 0; c < 32; c += 8) {
+            float4 a0 = arow[(c0 + c) / 4];
+            float4 a1 = arow[(c0 + c) / 4 + 1];
+            if (!keep) {
+              a0 = make_float4(fmaf(__uint_as_float(orow[c]), wb, a0.x * wa),
+                               fmaf(__uint_as_float(orow[c + 1]), wb, a0.y * wa),
+                               fmaf(__uint_as_float(orow[c + 2]), wb, a0.z * wa),
+                               fmaf(__uint_as_float(orow[c + 3]), wb, a0.w * wa));
+              a1 = make_float4(fmaf(__uint_as_float(orow[c + 4]), wb, a1.x * wa),
+                               fmaf(__uint_as_float(orow[c + 5]), wb, a1.y * wa),
+                               fmaf(__uint_as_float(orow[c + 6]), wb, a1.z * wa),
+                               fmaf(__uint_as_float(orow[c + 7]), wb, a1.w * wa));
+              *reinterpret_cast<float4*>(acc + c) = a0;
+              *reinterpret_cast<float4*>(acc + c + 4) = a1;
             }
-          } else {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out.ptr) + b * p.out.sn +
-                                 (int64_t)qi * p.out.sl + hq * p.out.sh + c0;
-#pragma unroll
-            for (int c = 0; c < 32; c += 8) {
+            if (p.fin.ptr != nullptr) {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.fin.ptr) + b * p.fin.sn +
+                                   (int64_t)qi * p.fin.sl + hq * p.fin.sh + c0 + c;
               uint4 v4;
-              v4.x = pack_bf16x2(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv);
-              v4.y = pack_bf16x2(__uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
-              v4.z = pack_bf16x2(__uint_as_float(orow[c + 4]) * inv, __uint_as_float(orow[c + 5]) * inv);
-              v4.w = pack_bf16x2(__uint_as_float(orow[c + 6]) * inv, __uint_as_float(orow[c + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + c) = v4;
+              v4.x = pack_bf16x2(a0.x, a0.y);
+              v4.y = pack_bf16x2(a0.z, a0.w);
+              v4.z = pack_bf16x2(a1.x, a1.y);
+              v4.w = pack_bf16x2(a1.z, a1.w);
+              *reinterpret_cast<uint4*>(dst) = v4;
             }
+          }
+        } else if (p.out_is_f32) {
+          float* dst = reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn + (int64_t)qi * p.out.sl +
+                       hq * p.out.sh + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 v4 = make_float4(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv,
+                                          __uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
+            *reinterpret_cast<float4*>(dst + c) = v4;
+          }
+        } else {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out.ptr) + b * p.out.sn +
+                               (int64_t)qi * p.out.sl + hq * p.out.sh + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v4;
+            v4.x = pack_bf16x2(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv);
+            v4.y = pack_bf16x2(__uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
+            v4.z = pack_bf16x2(__uint_as_float(orow[c + 4]) * inv, __uint_as_float(orow[c + 5]) * inv);
+            v4.w = pack_bf16x2(__uint_as_float(orow[c + 6]) * inv, __uint_as_float(orow[c + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c) = v4;
           }
         }
       }
-      if (row_ok) {
-        const float L = (l_sum > 0.f) ? (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f : -INFINITY;
-        p.lse.ptr[b * p.lse.sn + hq * p.lse.sh + qi] = L;
-      }
+      if (row_ok && !keep) *lse_p = l_new;
     }
   }
 
@@ -470,24 +525,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kMerge>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t s, int* nlaunch) {
   using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split above is only sound at exactly kRegsLaunch registers
   // per thread; refuse to launch otherwise (setmaxnreg.inc would never return).
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D>);
+  e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D, kMerge>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const int nqb = (p.a.lq + kSub * kBlockM - 1) / (kSub * kBlockM);
   const long long blocks = (long long)nqb * p.a.n * p.a.h;
   if (blocks == 0) return cudaSuccess;
   const float scale_log2 = p.a.scale * 1.4426950408889634f;
-  fwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, p, scale_log2);
+  fwd_bf16_kernel<D, kMerge><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, p, scale_log2);
   *nlaunch += 1;
   return cudaGetLastError();
 }
@@ -496,8 +551,10 @@ cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtens
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t s, int* nlaunch) {
-  if (p.a.d == 128) return launch_fwd_d<128>(p, tq, tk, tv, s, nlaunch);
-  if (p.a.d == 64) return launch_fwd_d<64>(p, tq, tk, tv, s, nlaunch);
+  if (p.a.d == 128) return p.merge ? launch_fwd_d<128, true>(p, tq, tk, tv, s, nlaunch)
+                                   : launch_fwd_d<128, false>(p, tq, tk, tv, s, nlaunch);
+  if (p.a.d == 64) return p.merge ? launch_fwd_d<64, true>(p, tq, tk, tv, s, nlaunch)
+                                  : launch_fwd_d<64, false>(p, tq, tk, tv, s, nlaunch);
   return cudaErrorInvalidValue;
 }
 

@@ -72,6 +72,22 @@ def flash_mha_fwd(q, k, v, softmax_scale=None, is_causal=False, window_size=(-1,
     return out, lse
 
 
+def flash_mha_fwd_merge(q, k, v, out_acc, lse_acc, softmax_scale=None, is_causal=False, window_size=(-1, -1),
+                        out_final=None):
+    """Fused ring step: the forward of (q, k, v) folded into the fp32
+    accumulator (out_acc, lse_acc) in place by the log-sum-exp merge;
+    ``out_final`` (bf16) also receives the merged rows."""
+    lib = _lib.load()
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[3])
+    ds = [_desc(x) for x in (q, k, v, out_acc, lse_acc, out_final)]
+    rc = lib.bea_flash_mha_fwd_merge(*[_ref(x) for x in ds], float(softmax_scale), int(bool(is_causal)),
+                                     int(window_size[0]), int(window_size[1]), _stream())
+    _lib.check(rc, "flash_mha_fwd_merge")
+    _count()
+    return out_acc, lse_acc
+
+
 def bwd_workspace_bytes(q) -> int:
     n, lq, h, d = q.shape
     return int(_lib.load().bea_flash_mha_bwd_workspace_size(n, lq, h, d))

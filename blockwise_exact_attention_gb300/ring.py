@@ -51,21 +51,63 @@ def _chunks(x, n_chunks, dim):
     return [x.narrow(dim, i * c, c) for i in range(n_chunks)]
 
 
+def _step_view(x, first: int, count: int, c: int, l_dim: int):
+    """Chunks first .. first + count - 1 of a batch-1 sequence tensor as one batch of
+    ``count`` chunks: [1, l, h, d] -> [count, c, h, d] (l_dim 1) or [1, h, l] ->
+    [count, h, c] (l_dim 2). A zero-copy strided view: the batch stride is one chunk."""
+    st = list(x.stride())
+    size = list(x.shape)
+    size[0], size[l_dim] = count, c
+    st[0] = c * x.stride(l_dim)
+    return x.as_strided(size, st, x.storage_offset() + first * c * x.stride(l_dim))
+
+
+def _ring_step_groups(n_chunks: int, is_causal: bool, cast: bool):
+    """Per ring step t, the calls that cover its chunk pairs: (first query chunk, first K/V
+    chunk, number of consecutive chunks, whether this is those query chunks' last step).
+    Step t pairs query chunk i with K/V chunk (i - t) mod C; under a causal mask the
+    wrapped pairs are skipped and query chunk i's last step is t = i, so when the result is
+    cast at the last step that chunk gets a call of its own."""
+    C = n_chunks
+    groups = []
+    for t in range(C):
+        if is_causal:
+            if cast:
+                parts = [(t, 0, 1, True)] + ([(t + 1, 1, C - 1 - t, False)] if C - 1 - t > 0 else [])
+            else:
+                parts = [(t, 0, C - t, False)]
+        else:
+            parts = [(t, 0, C - t, t == C - 1)] + ([(0, C - t, t, t == C - 1)] if t > 0 else [])
+        groups.append(parts)
+    return groups
+
+
 def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=True, out_dtype=None,
-                       block_dtype=None):
+                       block_dtype=None, fused=None):
     """Forward over ring chunk steps -> (out, lse).
 
     ``out_dtype`` fp32 makes the fp32 accumulator itself the result;
     otherwise (default: q's dtype) the last merge of each query chunk also
     writes the cast result. ``block_dtype`` is the dtype of each block's
     partial output (default: q's dtype, as the pages feed the kernel's
-    q-dtype output into the fp32 merge).
+    q-dtype output into the fp32 merge). ``fused`` (default: on for bf16
+    inputs when no block dtype is asked for) folds each block into the
+    accumulator inside the forward kernel instead of writing it out and
+    running ring_merge.
+
+    Every query chunk steps through its K/V chunks in ring order. On one GPU
+    the query chunks are independent, so all chunk pairs of one ring step run
+    as one call over a batch of chunk views (ring step t pairs query chunk i
+    with K/V chunk i - t): n_chunks launches (plus merges) instead of one per
+    chunk pair. Batches larger than 1 run their rows one after another.
     """
     n, l, h, d = q.shape
     if l % n_chunks:
         raise ValueError("sequence length must split evenly into chunks")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
+    if fused is None:
+        fused = q.dtype == torch.bfloat16 and block_dtype is None
     out_dtype = out_dtype or q.dtype
     block_dtype = block_dtype or q.dtype
     dev = q.device
@@ -73,23 +115,27 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
     lse = torch.empty((n, h, l), dtype=torch.float32, device=dev)
     acc = out if out_dtype == torch.float32 else torch.empty(q.shape, dtype=torch.float32, device=dev)
     c = l // n_chunks
-    qs, ks, vs = _chunks(q, n_chunks, 1), _chunks(k, n_chunks, 1), _chunks(v, n_chunks, 1)
-    accs, outs, lses = _chunks(acc, n_chunks, 1), _chunks(out, n_chunks, 1), _chunks(lse, n_chunks, 2)
-    blk = torch.empty((n, c, h, d), dtype=block_dtype, device=dev)
-    lse_blk = torch.empty((n, h, c), dtype=torch.float32, device=dev)
-    for i, steps in enumerate(chunk_schedule(n_chunks, is_causal)):
-        live = [(t, j, kind) for (t, j, kind) in steps if kind != "skip"]
-        for s, (_t, j, kind) in enumerate(live):
-            causal = kind == "causal"
-            last = s == len(live) - 1
-            if s == 0:
-                # the first block initialises the accumulator (merge with (0, -inf) is the identity)
-                target = outs[i] if (last and out_dtype != torch.float32) else accs[i]
-                ops.flash_mha_fwd(qs[i], ks[j], vs[j], softmax_scale, causal, out=target, lse=lses[i])
-            else:
-                ops.flash_mha_fwd(qs[i], ks[j], vs[j], softmax_scale, causal, out=blk, lse=lse_blk)
-                fin = outs[i] if (last and out_dtype != torch.float32) else None
-                ops.ring_merge(accs[i], lses[i], blk, lse_blk, out_final=fin)
+    cast = out_dtype != torch.float32
+    for b in range(n):
+        qb, kb, vb = q[b:b + 1], k[b:b + 1], v[b:b + 1]
+        accb, outb, lseb = acc[b:b + 1], out[b:b + 1], lse[b:b + 1]
+        for t, parts in enumerate(_ring_step_groups(n_chunks, is_causal, cast)):
+            for (i0, j0, cnt, final) in parts:
+                qv, kv_, vv = (_step_view(x_, f, cnt, c, 1) for x_, f in ((qb, i0), (kb, j0), (vb, j0)))
+                av, lv = _step_view(accb, i0, cnt, c, 1), _step_view(lseb, i0, cnt, c, 2)
+                fin = _step_view(outb, i0, cnt, c, 1) if (final and cast) else None
+                causal = is_causal and t == 0
+                if t == 0:
+                    # the first block initialises the accumulator (merge with (0, -inf) is the
+                    # identity); a chunk whose only block this is gets its final output at once
+                    ops.flash_mha_fwd(qv, kv_, vv, softmax_scale, causal, out=fin if fin is not None else av, lse=lv)
+                elif fused:
+                    ops.flash_mha_fwd_merge(qv, kv_, vv, av, lv, softmax_scale, causal, out_final=fin)
+                else:
+                    blk = torch.empty((cnt, c, h, d), dtype=block_dtype, device=dev)
+                    lblk = torch.empty((cnt, h, c), dtype=torch.float32, device=dev)
+                    ops.flash_mha_fwd(qv, kv_, vv, softmax_scale, causal, out=blk, lse=lblk)
+                    ops.ring_merge(av, lv, blk, lblk, out_final=fin)
     return out, lse
 
 

@@ -104,6 +104,28 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
                       int window_right, void* stream);
 
 /*
+ * Fused ring step: the forward of one K/V block, folded straight into a
+ * running fp32 accumulator by the log-sum-exp merge (flash_attn_jax
+ * flash_sharding.py, "Ring Forward": the block's (out, lse) merged into the
+ * carried (o, lse) once per ring step). Equal to bea_flash_mha_fwd into a
+ * temporary followed by bea_ring_merge, without writing the block's output
+ * to memory and without its rounding to bf16.
+ *
+ *   q, k, v    as for the forward, bf16 only (f32: BEA_ERR_UNSUPPORTED)
+ *   out_acc    [n, lq, h, d] f32, read and written
+ *   lse_acc    [n, h, lq]    f32, read and written
+ *   out_final  NULL, or [n, lq, h, d] bf16: also receives the merged rows cast
+ *              to bf16 (the last step of a ring)
+ * Per row, with La the accumulator's and L the block's log-sum-exp:
+ * M = max(La, L); if M == -inf the row is left unchanged; otherwise
+ * L' = M + log1p(exp(min(La, L) - M)), out_acc <- exp(La - L') out_acc +
+ * exp(L - L') O_block, lse_acc <- L'.
+ */
+int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,
+                            const bea_tensor* lse_acc, const bea_tensor* out_final, float softmax_scale, int is_causal,
+                            int window_left, int window_right, void* stream);
+
+/*
  * Bytes of device workspace bea_flash_mha_bwd needs for q of shape
  * [n, lq, h, d] (an fp32 dQ accumulator plus two fp32 values per row).
  */

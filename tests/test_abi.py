@@ -168,6 +168,23 @@ def test_staged_bwd_rejects_bad_arguments(lib):
     assert fin(dq=T([1, 256, 4, 64], F32), wsb=lib.bea_flash_mha_bwd_workspace_size(1, 256, 4, 64) - 1) == WS
 
 
+def test_fwd_merge_rejects_bad_arguments(lib):
+    q, k, v, o, l = good()
+    r = ctypes.byref
+    acc = T([1, 256, 4, 128], F32)
+
+    def call(q=q, k=k, acc=acc, lse=l, fin=None):
+        return lib.bea_flash_mha_fwd_merge(r(q), r(k), r(v), r(acc), r(lse), r(fin) if fin is not None else None,
+                                           0.125, 1, -1, -1, None)
+
+    assert call(acc=T([1, 256, 4, 128], BF16)) == DTYPE          # the accumulator is fp32
+    assert call(acc=T([1, 255, 4, 128], F32)) == SHAPE
+    assert call(lse=T([1, 4, 255], F32)) == SHAPE
+    assert call(fin=T([1, 256, 4, 128], F32)) == DTYPE           # the final copy is bf16
+    assert call(q=T([1, 256, 4, 128], F32), k=T([1, 256, 2, 128], F32)) == DTYPE  # v stays bf16
+    assert call(acc=T([1, 256, 4, 128], F32, ptr=FAKE + 4)) == ALIGN
+
+
 def test_merge_rejects_bad_arguments(lib):
     r = ctypes.byref
     acc, la = T([1, 64, 2, 128], F32), T([1, 2, 64], F32)

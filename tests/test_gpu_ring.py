@@ -1,6 +1,7 @@
 """Ring attention replayed as chunk steps on one GPU: forward chunk steps
-folded with ring_merge, and chunk-pair backward accumulation, checked against
-the single-call kernels (both with fp32 outputs, <= 1e-3) and the oracle."""
+folded with ring_merge or with the fused ring step (flash_mha_fwd_merge), and
+chunk-pair backward accumulation, checked against the single-call kernels
+(both with fp32 outputs, <= 1e-3) and the oracle."""
 
 import math
 
@@ -60,7 +61,8 @@ def test_ring_small(causal):
 
 
 def test_ring_full_size():
-    """[1, 16384, 16, 128] as 8 chunks of 2048: 36 chunk forwards, 28 merges."""
+    """[1, 16384, 16, 128] as 8 chunks of 2048: the 36 chunk-pair forwards and 28 merges run as one
+    batched call per ring step (8 forwards + 7 merges)."""
     import blockwise_exact_attention_gb300 as bea
     w = workloads.WORKLOADS["ring_causal_16k"]
     x = cached_inputs("ring_causal_16k")
@@ -69,15 +71,23 @@ def test_ring_full_size():
     bea.launches_since_reset(reset=True)
     ro32, rl32 = bea.ring_attention_fwd(q, k, v, w.ring_chunks, s, True, out_dtype=torch.float32,
                                         block_dtype=torch.float32)
-    assert bea.launches_since_reset(reset=True) == 36 + 28
+    assert bea.launches_since_reset(reset=True) == 8 + 7
     so32, sl32 = bea.flash_mha_fwd(q, k, v, s, True, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert_close(to_np(ro32), to_np(so32), TOL_RING, "ring vs single out (fp32)")
     assert_close(to_np(rl32), to_np(sl32), TOL_RING, "ring vs single lse")
-    # the bf16 mode rounds every block to bf16 before the merge (as the pages
-    # feed the kernel's q-dtype output into the fp32 accumulator), so its
-    # result is held to the bf16 tolerance against the single call
+    fo32, fl32 = bea.ring_attention_fwd(q, k, v, w.ring_chunks, s, True, out_dtype=torch.float32, fused=True)
+    torch.cuda.synchronize()
+    assert_close(to_np(fo32), to_np(so32), TOL_RING, "fused ring vs single out (fp32)")
+    assert_close(to_np(fl32), to_np(sl32), TOL_RING, "fused ring vs single lse")
+    del fo32, fl32
+    # the bf16 result (fused ring steps, cast at the last step) is held to the
+    # bf16 tolerance against the single call
+    bea.launches_since_reset(reset=True)
     rob, rlb = bea.ring_attention_fwd(q, k, v, w.ring_chunks, s, True)
+    # fused, cast to bf16 at each query chunk's last step: per causal step, the chunk that ends
+    # there and the rest (2 * 8 - 1 launches, no merge launches)
+    assert bea.launches_since_reset(reset=True) == 15
     sob, _ = bea.flash_mha_fwd(q, k, v, s, True)
     torch.cuda.synchronize()
     assert float(np.abs(to_np(rob) - to_np(sob)).max()) <= 2e-2
@@ -93,4 +103,78 @@ def test_ring_full_size():
     torch.cuda.synchronize()
     for name, a, b in zip(("dq", "dk", "dv"), rg, sg):
         assert_close(to_np(a), to_np(b), TOL_RING, name + " ring vs single")
+    assert bea.device_status() == 0
+
+
+# ---- the fused ring step --------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_merge_two_key_blocks(d):
+    """Forward of keys [0, 256) into an fp32 accumulator, then the fused step with keys
+    [256, 520): equals attention over all keys (oracle), and out_final is its bf16 cast."""
+    import blockwise_exact_attention_gb300 as bea
+    lq, lk, cut = 300, 520, 256
+    x = workloads.small_case(n=1, l=lq, h=4, h_kv=2, d=d, is_causal=False, seed=40 + d, lk=lk)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (to_dev(x[s_], torch.bfloat16) for s_ in ("q", "k", "v"))
+    acc, lse = bea.flash_mha_fwd(q, k[:, :cut], v[:, :cut], scale, False, out_dtype=torch.float32)
+    fin = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    bea.flash_mha_fwd_merge(q, k[:, cut:], v[:, cut:], acc, lse, scale, False, out_final=fin)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    ro, rl = oracle.attention_fwd(x["q"], x["k"], x["v"], scale, False)
+    assert_close_bf16(to_np(acc), ro, "merged out", output_is_bf16=False)
+    assert_close(to_np(lse), rl, TOL_LSE, "merged lse")
+    assert torch.equal(fin, acc.to(torch.bfloat16))
+    # the same fold through the oracle's merge of the two blocks
+    oa, la = oracle.attention_fwd(x["q"], x["k"][:, :cut], x["v"][:, :cut], scale, False)
+    ob, lb = oracle.attention_fwd(x["q"], x["k"][:, cut:], x["v"][:, cut:], scale, False)
+    om, lm = oracle.merge_max_form(oa, la, ob, lb)
+    assert_close_bf16(to_np(acc), om, "merged out vs oracle merge", output_is_bf16=False)
+
+
+def test_fwd_merge_minus_inf_rows():
+    """Accumulator rows at lse = -inf take the block exactly; an empty block leaves the
+    accumulator unchanged (both -inf: unchanged, lse stays -inf)."""
+    import blockwise_exact_attention_gb300 as bea
+    x = workloads.small_case(n=1, l=200, h=2, h_kv=1, d=128, is_causal=False, seed=45)
+    scale = 1.0 / math.sqrt(128)
+    q, k, v = (to_dev(x[s_], torch.bfloat16) for s_ in ("q", "k", "v"))
+    ref, ref_l = bea.flash_mha_fwd(q, k, v, scale, False, out_dtype=torch.float32)
+    acc = torch.randn(q.shape, device="cuda")
+    lse = torch.full((1, 2, 200), float("-inf"), device="cuda")
+    bea.flash_mha_fwd_merge(q, k, v, acc, lse, scale, False)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, ref) and torch.equal(lse, ref_l)
+    acc2 = torch.randn(q.shape, device="cuda")
+    keep = acc2.clone()
+    lse2 = torch.full((1, 2, 200), float("-inf"), device="cuda")
+    empty = torch.zeros((1, 0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    bea.flash_mha_fwd_merge(q, empty, empty, acc2, lse2, scale, False)
+    torch.cuda.synchronize()
+    assert torch.equal(acc2, keep) and bool(torch.isneginf(lse2).all())
+    assert bea.device_status() == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_fused_equals_unfused(causal):
+    """The fused ring step computes exactly the forward + ring_merge of fp32 blocks (to fp32
+    rounding), with one batched launch per ring step; against the oracle it holds the bf16-path
+    tolerance. (Ring vs single call differs by ~1e-3 on any chunking, since the two round P to
+    bf16 under different running maxima; the <= 1e-3 check runs on the 16k ring workload.)"""
+    import blockwise_exact_attention_gb300 as bea
+    x = workloads.small_case(n=1, l=1536, h=4, h_kv=1, d=128, is_causal=causal, seed=46)
+    scale = 1.0 / math.sqrt(128)
+    q, k, v = (to_dev(x[s_], torch.bfloat16) for s_ in ("q", "k", "v"))
+    bea.launches_since_reset(reset=True)
+    fo, fl = bea.ring_attention_fwd(q, k, v, 6, scale, causal, out_dtype=torch.float32, fused=True)
+    # one batched call per ring step (non-causal: the wrapped pairs of a step are a second call)
+    assert bea.launches_since_reset(reset=True) == (6 if causal else 11)
+    uo, ul = bea.ring_attention_fwd(q, k, v, 6, scale, causal, out_dtype=torch.float32, block_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_close(to_np(fo), to_np(uo), 1e-5, "fused vs unfused out")
+    assert_close(to_np(fl), to_np(ul), 1e-5, "fused vs unfused lse")
+    oo, ol = oracle.ring_fwd_replay(x["q"], x["k"], x["v"], scale, 6, causal)
+    assert_close_bf16(to_np(fo), oo, "fused ring out", output_is_bf16=False)
+    assert_close(to_np(fl), ol, TOL_LSE, "fused ring lse")
     assert bea.device_status() == 0
