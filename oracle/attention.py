@@ -24,7 +24,7 @@ so no step of the blocked algorithm is replayed here:
   K/V chunk index with the query chunk index, K/V moving i -> i+1 each step):
   ``flash_sharding.py`` "Ring Forward" and "Ring Backward".
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * window ``(left, right)``: key j is visible to query i iff
   ``(left < 0 or j >= i - left) and (right < 0 or j <= i + right)``;
