@@ -11,6 +11,8 @@ Public API (all calls run in libbea.so's CUDA kernels on the current stream):
   step (a block's forward folded into the accumulator)
 * ``ring_attention_fwd / ring_attention_bwd``: ring attention replayed as
   chunk steps on one GPU.
+* ``flash_attention / ring_attention``: the same as torch.autograd functions
+  (the backward recomputed from the saved log-sum-exp).
 
 The seeded input generators live in ``workloads`` and import nothing else.
 """
@@ -28,3 +30,4 @@ from .ops import (  # noqa: F401
     selftest_wait_timeout,
 )
 from .ring import chunk_schedule, ring_attention_bwd, ring_attention_fwd  # noqa: F401
+from .autograd import flash_attention, ring_attention  # noqa: F401,E402
