@@ -28,7 +28,14 @@ Readings taken where the pages are silent:
 
 * window ``(left, right)``: key j is visible to query i iff
   ``(left < 0 or j >= i - left) and (right < 0 or j <= i + right)``;
-  ``is_causal`` means ``right = 0``. Causal/windowed calls need ``lq == lk``.
+  ``is_causal`` means ``right = 0``.
+* key positions: key j sits at position ``j + key_offset`` of the query
+  positions, and the window compares positions:
+  ``(left < 0 or j + key_offset >= i - left) and (right < 0 or j + key_offset <= i + right)``.
+  By default ``key_offset = lq - lk``: with ``lq != lk`` the last query row is
+  aligned with the last key (bottom-right alignment; the pages only use
+  ``lq == lk``, where the offset is 0). Ring chunk pairs pass the distance
+  between their key chunk and their query chunk.
 * a query row with no visible key has ``out = 0``, ``lse = -inf`` and zero
   gradients (the skipped-block convention of ``ring_fwd``, applied per row).
 * merging two rows that both have ``lse = -inf`` leaves the accumulator as it
@@ -75,15 +82,16 @@ def _effective_window(is_causal: bool, window: tuple[int, int]) -> tuple[int, in
 
 
 def visible_mask(rows: np.ndarray, lk: int, is_causal: bool,
-                 window: tuple[int, int] = (-1, -1)) -> np.ndarray:
+                 window: tuple[int, int] = (-1, -1), key_offset: int = 0) -> np.ndarray:
     """Boolean ``[len(rows), lk]``: True where query ``rows[r]`` may see key ``j``.
 
     Causal masking as in picotron ``ring_attention_forward`` (entries above the
-    diagonal are masked); the window is the reading stated in the module doc.
+    diagonal are masked); the window and the key offset are the readings stated
+    in the module doc.
     """
     left, right = _effective_window(is_causal, window)
     i = np.asarray(rows, dtype=np.int64)[:, None]
-    j = np.arange(lk, dtype=np.int64)[None, :]
+    j = np.arange(lk, dtype=np.int64)[None, :] + int(key_offset)
     vis = np.ones((i.shape[0], lk), dtype=bool)
     if left >= 0:
         vis &= j >= i - left
@@ -93,13 +101,18 @@ def visible_mask(rows: np.ndarray, lk: int, is_causal: bool,
 
 
 def _key_band(r0: int, r1: int, lk: int, is_causal: bool,
-              window: tuple[int, int]) -> tuple[int, int]:
+              window: tuple[int, int], key_offset: int = 0) -> tuple[int, int]:
     """Keys that any of the query rows ``[r0, r1)`` can see (all others are
     masked, so dropping them changes no sum)."""
     left, right = _effective_window(is_causal, window)
-    k0 = 0 if left < 0 else max(0, r0 - left)
-    k1 = lk if right < 0 else min(lk, r1 - 1 + right + 1)
+    k0 = 0 if left < 0 else min(lk, max(0, r0 - left - key_offset))
+    k1 = lk if right < 0 else max(0, min(lk, r1 - 1 + right - key_offset + 1))
     return k0, max(k0, k1)
+
+
+def _key_offset(lq: int, lk: int, key_offset) -> int:
+    """The default key offset: bottom-right alignment (0 when lq == lk)."""
+    return lq - lk if key_offset is None else int(key_offset)
 
 
 def _check_shapes(q, k, v, is_causal, window):
@@ -111,9 +124,7 @@ def _check_shapes(q, k, v, is_causal, window):
         raise ValueError("k, v must be [n, lk, h_kv, d] matching q")
     if hkv == 0 or h % hkv != 0:
         raise ValueError("h must be a multiple of h_kv")
-    left, right = _effective_window(is_causal, window)
-    if (is_causal or left >= 0 or right >= 0) and lq != lk:
-        raise ValueError("causal / windowed attention needs lq == lk")
+    _effective_window(is_causal, window)
     return n, lq, lk, h, hkv, d
 
 
@@ -123,7 +134,7 @@ def _check_shapes(q, k, v, is_causal, window):
 
 def attention_fwd(q, k, v, softmax_scale: float, is_causal: bool = False,
                   window: tuple[int, int] = (-1, -1), rows=None,
-                  row_block: int = 1024):
+                  row_block: int = 1024, key_offset=None):
     """Exact attention forward in fp64: returns ``(out [n,l,h,d], lse [n,h,l])``.
 
     For each batch b and query head hq (K/V head ``hq // g``):
@@ -133,11 +144,14 @@ def attention_fwd(q, k, v, softmax_scale: float, is_causal: bool = False,
 
     ``rows`` (optional) restricts the computation to those absolute query row
     indices; the result then has ``len(rows)`` rows in place of ``lq``.
+    ``key_offset`` places key j at query position ``j + key_offset`` (default:
+    ``lq - lk``, bottom-right alignment).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     n, lq, lk, h, hkv, d = _check_shapes(q, k, v, is_causal, window)
+    off = _key_offset(lq, lk, key_offset)
     g = h // hkv
     if rows is None:
         rows = np.arange(lq, dtype=np.int64)
@@ -148,10 +162,10 @@ def attention_fwd(q, k, v, softmax_scale: float, is_causal: bool = False,
     for r0 in range(0, nr, row_block):
         r1 = min(nr, r0 + row_block)
         idx = rows[r0:r1]
-        k0, k1 = _key_band(int(idx.min()), int(idx.max()) + 1, lk, is_causal, window)
+        k0, k1 = _key_band(int(idx.min()), int(idx.max()) + 1, lk, is_causal, window, off)
         if k1 <= k0:
             continue
-        vis = visible_mask(idx, lk, is_causal, window)[:, k0:k1]
+        vis = visible_mask(idx, lk, is_causal, window, off)[:, k0:k1]
         any_vis = vis.any(axis=1)
         for b in range(n):
             for hq in range(h):
@@ -170,14 +184,14 @@ def attention_fwd(q, k, v, softmax_scale: float, is_causal: bool = False,
 
 
 def attention_probs(q, k, softmax_scale: float, is_causal: bool = False,
-                    window: tuple[int, int] = (-1, -1)):
+                    window: tuple[int, int] = (-1, -1), key_offset=None):
     """The full probability matrix ``P [n, h, lq, lk]`` (small inputs only)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     n, lq, h, d = q.shape
     lk, hkv = k.shape[1], k.shape[2]
     g = h // hkv
-    vis = visible_mask(np.arange(lq), lk, is_causal, window)
+    vis = visible_mask(np.arange(lq), lk, is_causal, window, _key_offset(lq, lk, key_offset))
     any_vis = vis.any(axis=1)
     P = np.zeros((n, h, lq, lk))
     for b in range(n):
@@ -197,7 +211,7 @@ def attention_probs(q, k, softmax_scale: float, is_causal: bool = False,
 
 def attention_bwd(dout, q, k, v, out, lse, softmax_scale: float,
                   is_causal: bool = False, window: tuple[int, int] = (-1, -1),
-                  row_block: int = 1024):
+                  row_block: int = 1024, key_offset=None):
     """Analytic backward in fp64 from the GIVEN ``out`` and ``lse``.
 
     ``P = exp(S - lse)`` (masked entries 0), ``dV = P^T dO``, ``dP = dO V^T``,
@@ -215,6 +229,7 @@ def attention_bwd(dout, q, k, v, out, lse, softmax_scale: float,
     out = np.asarray(out, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     n, lq, lk, h, hkv, d = _check_shapes(q, k, v, is_causal, window)
+    off = _key_offset(lq, lk, key_offset)
     g = h // hkv
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
@@ -222,10 +237,10 @@ def attention_bwd(dout, q, k, v, out, lse, softmax_scale: float,
     for r0 in range(0, lq, row_block):
         r1 = min(lq, r0 + row_block)
         idx = np.arange(r0, r1)
-        k0, k1 = _key_band(r0, r1, lk, is_causal, window)
+        k0, k1 = _key_band(r0, r1, lk, is_causal, window, off)
         if k1 <= k0:
             continue
-        vis = visible_mask(idx, lk, is_causal, window)[:, k0:k1]
+        vis = visible_mask(idx, lk, is_causal, window, off)[:, k0:k1]
         for b in range(n):
             for hq in range(h):
                 kv = hq // g
@@ -333,12 +348,14 @@ def ring_chunk_schedule(n_chunks: int, is_causal: bool):
     return sched
 
 
-def ring_fwd_replay(q, k, v, softmax_scale: float, n_chunks: int, is_causal: bool):
+def ring_fwd_replay(q, k, v, softmax_scale: float, n_chunks: int, is_causal: bool,
+                    window: tuple[int, int] = (-1, -1)):
     """Forward of ring attention on sequence chunks, folded with the merge.
 
     Each query chunk starts from the accumulator (0, -inf) and folds in the
     block result of every K/V chunk in ring order; skipped chunks contribute
-    (0, -inf).
+    (0, -inf). With a window, every chunk pair is masked by positions (its key
+    chunk placed at offset ``(j - i) * c`` from its query chunk).
     """
     q = np.asarray(q, dtype=np.float64)
     n, l, h, d = q.shape
@@ -353,10 +370,14 @@ def ring_fwd_replay(q, k, v, softmax_scale: float, n_chunks: int, is_causal: boo
         l_acc = np.full((n, h, c), NEG_INF)
         for _t, j, kind in steps:
             ks = slice(j * c, (j + 1) * c)
-            if kind == "skip":
+            if tuple(window) != (-1, -1):
+                o_b, l_b = attention_fwd(q[:, qs], k[:, ks], v[:, ks], softmax_scale, is_causal, window,
+                                         key_offset=(j - i) * c)
+            elif kind == "skip":
                 continue
-            o_b, l_b = attention_fwd(q[:, qs], k[:, ks], v[:, ks], softmax_scale,
-                                     is_causal=(kind == "causal"))
+            else:
+                o_b, l_b = attention_fwd(q[:, qs], k[:, ks], v[:, ks], softmax_scale,
+                                         is_causal=(kind == "causal"))
             o_acc, l_acc = merge_max_form(o_acc, l_acc, o_b, l_b)
         out[:, qs] = o_acc
         lse[:, :, qs] = l_acc
@@ -364,7 +385,7 @@ def ring_fwd_replay(q, k, v, softmax_scale: float, n_chunks: int, is_causal: boo
 
 
 def ring_bwd_replay(dout, q, k, v, out, lse, softmax_scale: float, n_chunks: int,
-                    is_causal: bool):
+                    is_causal: bool, window: tuple[int, int] = (-1, -1)):
     """Backward of ring attention: every visible chunk pair (i, j) runs the
     block backward with the FINAL out/lse of query chunk i, and the partial
     gradients are summed (flash_sharding.py, "Ring Backward"). One process
@@ -378,12 +399,17 @@ def ring_bwd_replay(dout, q, k, v, out, lse, softmax_scale: float, n_chunks: int
     for i, steps in enumerate(ring_chunk_schedule(n_chunks, is_causal)):
         qs = slice(i * c, (i + 1) * c)
         for _t, j, kind in steps:
-            if kind == "skip":
-                continue
             ks = slice(j * c, (j + 1) * c)
-            a, b_, c_ = attention_bwd(dout[:, qs], q[:, qs], k[:, ks], v[:, ks],
-                                      out[:, qs], lse[:, :, qs], softmax_scale,
-                                      is_causal=(kind == "causal"))
+            if tuple(window) != (-1, -1):
+                a, b_, c_ = attention_bwd(dout[:, qs], q[:, qs], k[:, ks], v[:, ks],
+                                          out[:, qs], lse[:, :, qs], softmax_scale,
+                                          is_causal, window, key_offset=(j - i) * c)
+            elif kind == "skip":
+                continue
+            else:
+                a, b_, c_ = attention_bwd(dout[:, qs], q[:, qs], k[:, ks], v[:, ks],
+                                          out[:, qs], lse[:, :, qs], softmax_scale,
+                                          is_causal=(kind == "causal"))
             dq[:, qs] += a
             dk[:, ks] += b_
             dv[:, ks] += c_

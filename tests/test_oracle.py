@@ -443,6 +443,12 @@ MUTATIONS = {
                           "o = out_a * _rows_view(wb) + out_b * _rows_view(wa)"),
     "lse_without_max": ("row_lse = np.where(any_vis, m + np.log(ssum), NEG_INF)",
                         "row_lse = np.where(any_vis, np.log(ssum), NEG_INF)"),
+    "key_offset_sign": ("j = np.arange(lk, dtype=np.int64)[None, :] + int(key_offset)",
+                        "j = np.arange(lk, dtype=np.int64)[None, :] - int(key_offset)"),
+    "top_left_alignment": ("return lq - lk if key_offset is None else int(key_offset)",
+                           "return 0 if key_offset is None else int(key_offset)"),
+    "key_band_offset_sign": ("k0 = 0 if left < 0 else min(lk, max(0, r0 - left - key_offset))",
+                             "k0 = 0 if left < 0 else min(lk, max(0, r0 - left + key_offset))"),
 }
 
 
@@ -483,6 +489,18 @@ def _pins_pass(mod):
             bo, bl, bdq, bdk, bdv = _brute(q, k, v, do, 0.7, causal, window)
             for a, b in zip((out, lse) + tuple(grads), (bo, bl, bdq, bdk, bdv)):
                 np.testing.assert_allclose(a, b, atol=1e-12)
+        # unequal lengths: explicit offsets and the default (bottom-right) alignment
+        q = _rand((1, 6, 2, 4), 71)
+        k = _rand((1, 9, 1, 4), 72)
+        v = _rand((1, 9, 1, 4), 73)
+        do = _rand((1, 6, 2, 4), 74)
+        for causal, window in MASKS:
+            for off in (-6, -2, None, 3):
+                out, lse = mod.attention_fwd(q, k, v, 0.6, causal, window, key_offset=off)
+                grads = mod.attention_bwd(do, q, k, v, out, lse, 0.6, causal, window, key_offset=off)
+                ref = _brute_offset(q, k, v, do, 0.6, causal, window, 6 - 9 if off is None else off)
+                for a, b in zip((out, lse) + tuple(grads), ref):
+                    np.testing.assert_allclose(a, b, atol=1e-12)
     except AssertionError:
         return False
     return True
@@ -495,3 +513,132 @@ def test_pins_pass_on_the_real_oracle():
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistakes(name):
     assert not _pins_pass(_mutant(name)), f"mutation {name} went unnoticed"
+
+
+# ---------------------------------------------------------------------------
+# key positions offset from query positions (lq != lk, ring chunk pairs)
+# ---------------------------------------------------------------------------
+
+def _brute_offset(q, k, v, do, scale, causal, window, off):
+    """Scalar loops with key j at query position j + off (the reading of the
+    module doc), any lq and lk."""
+    n, lq, h, d = q.shape
+    lk, hkv = k.shape[1], k.shape[2]
+    g = h // hkv
+    out = np.zeros_like(q)
+    lse = np.full((n, h, lq), -np.inf)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(n):
+        for hq in range(h):
+            kv = hq // g
+            for i in range(lq):
+                keys = [j for j in range(lk) if _bf_visible(i, j + off, causal, window)]
+                if not keys:
+                    continue
+                s = {j: scale * math.fsum(q[b, i, hq, c] * k[b, j, kv, c] for c in range(d)) for j in keys}
+                m = max(s.values())
+                z = math.fsum(math.exp(s[j] - m) for j in keys)
+                lse[b, hq, i] = m + math.log(z)
+                p = {j: math.exp(s[j] - m) / z for j in keys}
+                o = [math.fsum(p[j] * v[b, j, kv, c] for j in keys) for c in range(d)]
+                out[b, i, hq, :] = o
+                ds = {j: p[j] * math.fsum(do[b, i, hq, c] * (v[b, j, kv, c] - o[c]) for c in range(d))
+                      for j in keys}
+                for c in range(d):
+                    dq[b, i, hq, c] = scale * math.fsum(ds[j] * k[b, j, kv, c] for j in keys)
+                for j in keys:
+                    for c in range(d):
+                        dk[b, j, kv, c] += scale * ds[j] * q[b, i, hq, c]
+                        dv[b, j, kv, c] += p[j] * do[b, i, hq, c]
+    return out, lse, dq, dk, dv
+
+
+@pytest.mark.parametrize("causal,window", MASKS)
+@pytest.mark.parametrize("off", [-6, -2, 0, 3])
+def test_brute_force_key_offset(causal, window, off):
+    q = _rand((1, 6, 2, 4), 71)
+    k = _rand((1, 9, 1, 4), 72)
+    v = _rand((1, 9, 1, 4), 73)
+    do = _rand((1, 6, 2, 4), 74)
+    out, lse = oracle.attention_fwd(q, k, v, 0.6, causal, window, key_offset=off)
+    grads = oracle.attention_bwd(do, q, k, v, out, lse, 0.6, causal, window, key_offset=off)
+    ref = _brute_offset(q, k, v, do, 0.6, causal, window, off)
+    for got, want in zip((out, lse) + tuple(grads), ref):
+        np.testing.assert_allclose(got, want, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,window", MASKS)
+def test_bottom_right_is_the_suffix_of_the_square(causal, window):
+    """Default alignment for lq < lk: the last query row sees up to the last key, so the lq
+    rows are exactly the last lq rows of the square computation over all lk queries."""
+    lk, lq = 11, 4
+    q, k, v, do = _tiny(81, l=lk, h=2, hkv=1, d=4)
+    full_o, full_l = oracle.attention_fwd(q, k, v, 0.8, causal, window)
+    o, l_ = oracle.attention_fwd(q[:, lk - lq:], k, v, 0.8, causal, window)
+    np.testing.assert_allclose(o, full_o[:, lk - lq:], atol=1e-13)
+    np.testing.assert_allclose(l_, full_l[:, :, lk - lq:], atol=1e-13)
+    # dq of those rows does not depend on the other query rows
+    do_sfx = do[:, lk - lq:]
+    dq, _, _ = oracle.attention_bwd(do_sfx, q[:, lk - lq:], k, v, o, l_, 0.8, causal, window)
+    do_full = np.zeros_like(do)
+    do_full[:, lk - lq:] = do_sfx
+    fdq, _, _ = oracle.attention_bwd(do_full, q, k, v, full_o, full_l, 0.8, causal, window)
+    np.testing.assert_allclose(dq, fdq[:, lk - lq:], atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,window", [(True, (-1, -1)), (True, (5, 0)), (False, (4, 3))])
+def test_key_chunks_with_offsets_merge_to_the_whole(causal, window):
+    """Rows [a, b) of attention over all keys = the merge, over key chunks [c0, c1), of
+    attention of those rows against the chunk placed at offset c0 - a."""
+    l = 16
+    q, k, v, _ = _tiny(91, l=l, h=2, hkv=2, d=4)
+    full_o, full_l = oracle.attention_fwd(q, k, v, 0.7, causal, window)
+    a, b = 5, 12
+    acc_o = np.zeros((1, b - a, 2, 4))
+    acc_l = np.full((1, 2, b - a), -np.inf)
+    for c0, c1 in ((0, 3), (3, 8), (8, 13), (13, 16)):
+        o_, l_ = oracle.attention_fwd(q[:, a:b], k[:, c0:c1], v[:, c0:c1], 0.7, causal, window,
+                                      key_offset=c0 - a)
+        acc_o, acc_l = oracle.merge_max_form(acc_o, acc_l, o_, l_)
+    np.testing.assert_allclose(acc_o, full_o[:, a:b], atol=1e-12)
+    np.testing.assert_allclose(acc_l, full_l[:, :, a:b], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,window", [(True, (5, 0)), (False, (3, 2)), (True, (0, 0))])
+def test_windowed_ring_replay_matches_single_call(causal, window):
+    q, k, v, do = _tiny(95, l=24, h=2, hkv=1, d=4)
+    o, l_ = oracle.ring_fwd_replay(q, k, v, 0.5, 4, causal, window)
+    so, sl = oracle.attention_fwd(q, k, v, 0.5, causal, window)
+    np.testing.assert_allclose(o, so, atol=1e-12)
+    np.testing.assert_allclose(l_, sl, atol=1e-12)
+    g = oracle.ring_bwd_replay(do, q, k, v, so, sl, 0.5, 4, causal, window)
+    sg = oracle.attention_bwd(do, q, k, v, so, sl, 0.5, causal, window)
+    for a_, b_ in zip(g, sg):
+        np.testing.assert_allclose(a_, b_, atol=1e-12)
+
+
+def test_finite_differences_unequal_lengths():
+    q = _rand((1, 4, 2, 3), 101)
+    k = _rand((1, 7, 1, 3), 102)
+    v = _rand((1, 7, 1, 3), 103)
+    do = _rand((1, 4, 2, 3), 104)
+    out, lse = oracle.attention_fwd(q, k, v, 0.9, True, (2, 0))
+    grads = oracle.attention_bwd(do, q, k, v, out, lse, 0.9, True, (2, 0))
+
+    def f(qq, kk, vv):
+        return float(np.sum(do * oracle.attention_fwd(qq, kk, vv, 0.9, True, (2, 0))[0]))
+
+    eps = 1e-6
+    for which, (arr, grad) in enumerate(zip((q, k, v), grads)):
+        num = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [q.copy(), k.copy(), v.copy()]
+            minus = [q.copy(), k.copy(), v.copy()]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            num[idx] = (f(*plus) - f(*minus)) / (2 * eps)
+        assert np.max(np.abs(num - grad)) / max(1.0, np.max(np.abs(num))) < 1e-6, which
