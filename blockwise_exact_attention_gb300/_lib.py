@@ -80,7 +80,7 @@ def load() -> ctypes.CDLL:
     vp, i, f, sz, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_int64
     lib.bea_flash_mha_fwd.argtypes = [P, P, P, P, P, f, i, i, i, vp]
     lib.bea_flash_mha_fwd.restype = i
-    lib.bea_flash_mha_fwd_merge.argtypes = [P, P, P, P, P, P, f, i, i, i, vp]
+    lib.bea_flash_mha_fwd_merge.argtypes = [P, P, P, P, P, P, f, i, i, i, i64, vp]
     lib.bea_flash_mha_fwd_merge.restype = i
     lib.bea_flash_mha_bwd_workspace_size.argtypes = [i64, i64, i64, i64]
     lib.bea_flash_mha_bwd_workspace_size.restype = sz
@@ -102,7 +102,7 @@ def load() -> ctypes.CDLL:
     lib.bea_flash_mha_bwd_noalloc.restype = i
     lib.bea_flash_mha_bwd_prepare.argtypes = [P, P, P, vp, sz, vp]
     lib.bea_flash_mha_bwd_prepare.restype = i
-    lib.bea_flash_mha_bwd_kv_block.argtypes = [P, P, P, P, P, P, f, i, i, i, i, vp, sz, vp]
+    lib.bea_flash_mha_bwd_kv_block.argtypes = [P, P, P, P, P, P, f, i, i, i, i64, i, vp, sz, vp]
     lib.bea_flash_mha_bwd_kv_block.restype = i
     lib.bea_flash_mha_bwd_finish.argtypes = [P, f, i, vp, sz, vp]
     lib.bea_flash_mha_bwd_finish.restype = i

@@ -1,6 +1,7 @@
 // C ABI of libbea: argument validation, tensor-map construction and kernel
 // dispatch. Every check runs before any CUDA call, so a rejected request
 // touches neither the device nor the stream.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -101,18 +102,28 @@ bool same_shape(const bea_tensor* a, const bea_tensor* b) {
 Seq4 seq4(const bea_tensor* t) { return Seq4{t->data, t->stride[0], t->stride[1], t->stride[2]}; }
 Lse3 lse3(const bea_tensor* t) { return Lse3{static_cast<float*>(t->data), t->stride[0], t->stride[1]}; }
 
-int check_window(int is_causal, int wl, int wr, int* ewl, int* ewr) {
+// Fold the caller's window (-1 = unbounded), the causal flag (right = 0) and
+// the key position offset (key j sits at query position j + key_offset) into
+// the kernels' signed band: key j visible to query i iff i - ewl <= j <= i + ewr.
+int check_window(int is_causal, int wl, int wr, int64_t key_offset, int* ewl, int* ewr) {
   if (wl < -1 || wr < -1) return BEA_ERR_ARG;
   if (is_causal != 0 && is_causal != 1) return BEA_ERR_ARG;
   if (is_causal && wr > 0) return BEA_ERR_ARG;
-  *ewl = wl;
-  *ewr = is_causal ? 0 : wr;
+  if (key_offset < -(int64_t)bea::kUnbounded || key_offset > (int64_t)bea::kUnbounded) return BEA_ERR_ARG;
+  auto clamp = [](int64_t x) {
+    return (int)std::max<int64_t>(-bea::kUnbounded, std::min<int64_t>(bea::kUnbounded, x));
+  };
+  const int right = is_causal ? 0 : wr;
+  *ewl = (wl < 0) ? bea::kUnbounded : clamp((int64_t)wl + key_offset);
+  *ewr = (right < 0) ? bea::kUnbounded : clamp((int64_t)right - key_offset);
   return BEA_OK;
 }
 
 // Shared validation of q, k, v (and the mask) for forward and backward.
+// key_offset: the position of key 0 relative to query 0; nullptr = the
+// bottom-right alignment lq - lk (0 when lq == lk).
 int check_qkv(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, float scale, int is_causal, int wl,
-              int wr, AttnDims* a) {
+              int wr, const int64_t* key_offset, AttnDims* a) {
   int rc;
   if ((rc = check_tensor(q, 4)) || (rc = check_tensor(k, 4)) || (rc = check_tensor(v, 4))) return rc;
   if (q->dtype != k->dtype || q->dtype != v->dtype) return BEA_ERR_DTYPE;
@@ -121,9 +132,10 @@ int check_qkv(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, flo
   const int64_t h = q->shape[2], hkv = k->shape[2];
   if (hkv <= 0 || h % hkv != 0) return BEA_ERR_SHAPE;
   if (!std::isfinite(scale) || !(scale > 0.f)) return BEA_ERR_ARG;
+  if (q->shape[1] >= bea::kUnbounded || k->shape[1] >= bea::kUnbounded) return BEA_ERR_SHAPE;
+  const int64_t off = key_offset ? *key_offset : q->shape[1] - k->shape[1];
   int ewl, ewr;
-  if ((rc = check_window(is_causal, wl, wr, &ewl, &ewr))) return rc;
-  if ((ewl >= 0 || ewr >= 0) && q->shape[1] != k->shape[1]) return BEA_ERR_SHAPE;
+  if ((rc = check_window(is_causal, wl, wr, off, &ewl, &ewr))) return rc;
   const int64_t d = q->shape[3];
   if (q->dtype == BEA_BF16) {
     if (d != 64 && d != 128) return BEA_ERR_UNSUPPORTED;
@@ -251,7 +263,7 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
                       void* stream) {
   AttnDims a;
   int rc;
-  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, nullptr, &a))) return rc;
   if ((rc = check_tensor(out, 4))) return rc;
   if (!same_shape(out, q)) return BEA_ERR_SHAPE;
   if ((rc = check_lse(lse, a))) return rc;
@@ -283,10 +295,10 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
 
 int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,
                             const bea_tensor* lse_acc, const bea_tensor* out_final, float softmax_scale, int is_causal,
-                            int window_left, int window_right, void* stream) {
+                            int window_left, int window_right, int64_t key_offset, void* stream) {
   AttnDims a;
   int rc;
-  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &key_offset, &a))) return rc;
   if ((rc = check_tensor(out_acc, 4))) return rc;
   if (!same_shape(out_acc, q)) return BEA_ERR_SHAPE;
   if (out_acc->dtype != BEA_F32) return BEA_ERR_DTYPE;
@@ -329,7 +341,7 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
                       int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
   AttnDims a;
   int rc;
-  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, nullptr, &a))) return rc;
   if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(out, 4)) || (rc = check_tensor(dq, 4)) ||
       (rc = check_tensor(dk, 4)) || (rc = check_tensor(dv, 4)))
     return rc;
@@ -411,10 +423,11 @@ int bea_flash_mha_bwd_prepare(const bea_tensor* dout, const bea_tensor* out, con
 int bea_flash_mha_bwd_kv_block(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k,
                                const bea_tensor* v, const bea_tensor* dk, const bea_tensor* dv,
                                float softmax_scale, int is_causal, int window_left, int window_right,
-                               int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+                               int64_t key_offset, int accumulate, void* workspace, size_t workspace_bytes,
+                               void* stream) {
   AttnDims a;
   int rc;
-  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &a))) return rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, &key_offset, &a))) return rc;
   if (q->dtype != BEA_BF16) return BEA_ERR_UNSUPPORTED;
   if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(dk, 4)) || (rc = check_tensor(dv, 4))) return rc;
   if (!same_shape(dout, q) || !same_shape(dk, k) || !same_shape(dv, k)) return BEA_ERR_SHAPE;

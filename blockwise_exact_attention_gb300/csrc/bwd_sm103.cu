@@ -201,8 +201,8 @@ struct BwdSched {
 
 __device__ __forceinline__ bool bwd_tile_needs_mask(const AttnDims& a, int k0, int q0) {
   if (k0 + kBN - 1 >= a.lk) return true;
-  if (a.wl >= 0 && k0 < q0 + kBM - 1 - a.wl) return true;
-  if (a.wr >= 0 && k0 + kBN - 1 > q0 + a.wr) return true;
+  if ((long long)k0 < (long long)q0 + kBM - 1 - a.wl) return true;
+  if ((long long)k0 + kBN - 1 > (long long)q0 + a.wr) return true;
   return false;
 }
 
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.g = a.h / a.hkv;
   {
     const int k1 = min(sc.k0 + kBN, a.lk) - 1;
-    const int qmin = (a.wr < 0) ? 0 : max(0, sc.k0 - a.wr);
-    const int qmax = (a.wl < 0) ? a.lq : min(a.lq, k1 + a.wl + 1);
+    const int qmin = (int)max(0LL, (long long)sc.k0 - a.wr);
+    const int qmax = (int)min((long long)a.lq, (long long)k1 + a.wl + 1);
     if (qmax > qmin) {
       sc.i_lo = qmin / kBM;
       sc.i_hi = (qmax + kBM - 1) / kBM;

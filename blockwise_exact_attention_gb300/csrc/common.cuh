@@ -20,15 +20,21 @@ struct Lse3 {
   int64_t sn, sh;
 };
 
+// Bound of the visible band meaning "no limit"; sequence lengths stay below it.
+constexpr int kUnbounded = 1 << 30;
+
 struct AttnDims {
   int n, lq, lk, h, hkv, d;
-  int wl, wr;  // effective window: -1 unbounded; causal already folded into wr = 0
+  // Visible band, in key indices relative to the query index: key j is visible
+  // to query i iff i - wl <= j <= i + wr. The host folds the caller's window,
+  // the causal flag and the key position offset into these signed bounds
+  // (kUnbounded: no limit on that side).
+  int wl, wr;
   float scale;
 };
 
-// Key j is visible to query i (inclusive window reading; causal = right 0).
 __host__ __device__ __forceinline__ bool key_visible(int i, int j, int wl, int wr) {
-  return (wl < 0 || j >= i - wl) && (wr < 0 || j <= i + wr);
+  return j >= i - wl && j <= i + wr;
 }
 
 // ---- ring merge --------------------------------------------------------------

@@ -78,8 +78,8 @@ __device__ __forceinline__ void tile_range(const AttnDims& a, int qs, int& lo, i
   lo = hi = 0;
   if (qs >= a.lq) return;
   const int qe = min(qs + kBlockM, a.lq);
-  const int kmin = (a.wl < 0) ? 0 : max(0, qs - a.wl);
-  const int kmax = (a.wr < 0) ? a.lk : min(a.lk, qe - 1 + a.wr + 1);
+  const int kmin = (int)max(0LL, (long long)qs - a.wl);
+  const int kmax = (int)min((long long)a.lk, (long long)qe + a.wr);
   if (kmax <= kmin) return;
   lo = kmin / kBlockN;
   hi = (kmax + kBlockN - 1) / kBlockN;
@@ -90,8 +90,8 @@ __device__ __forceinline__ bool tile_needs_mask(const AttnDims& a, int qs, int j
   const int k0 = j * kBlockN, k1 = k0 + kBlockN - 1;
   if (k1 >= a.lk) return true;
   const int q1 = qs + kBlockM - 1;
-  if (a.wl >= 0 && k0 < q1 - a.wl) return true;
-  if (a.wr >= 0 && k1 > qs + a.wr) return true;
+  if ((long long)k0 < (long long)q1 - a.wl) return true;
+  if ((long long)k1 > (long long)qs + a.wr) return true;
   return false;
 }
 

@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(F32FwdParams p) {
   if (row_ok)
     for (int c = lane; c < d; c += 32) sQ[warp][c] = row_ptr(p.q, b, i, hq)[c];
   const int last = min(a.lq - 1, i0 + kWarps - 1);
-  const int j_lo = (a.wl < 0) ? 0 : max(0, i0 - a.wl);
-  const int j_hi = (a.wr < 0) ? a.lk : min(a.lk, last + a.wr + 1);
+  const int j_lo = (int)max(0LL, (long long)i0 - a.wl);
+  const int j_hi = (int)max((long long)j_lo, min((long long)a.lk, (long long)last + a.wr + 1));
   float m = -INFINITY, l = 0.f;
   float acc[kMaxD / 32];
 #pragma unroll
@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_f32_dq_kernel(F32BwdParams p)
     Dv = p.D[((int64_t)b * a.h + hq) * a.lq + i];
   }
   const int last = min(a.lq - 1, i0 + kWarps - 1);
-  const int j_lo = (a.wl < 0) ? 0 : max(0, i0 - a.wl);
-  const int j_hi = (a.wr < 0) ? a.lk : min(a.lk, last + a.wr + 1);
+  const int j_lo = (int)max(0LL, (long long)i0 - a.wl);
+  const int j_hi = (int)max((long long)j_lo, min((long long)a.lk, (long long)last + a.wr + 1));
   float acc[kMaxD / 32];
 #pragma unroll
   for (int t = 0; t < kMaxD / 32; ++t) acc[t] = 0.f;
@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_f32_dkv_kernel(F32BwdParams p
       sV[warp][c] = row_ptr(p.v, b, j, kvh)[c];
     }
   const int jlast = min(a.lk - 1, j0 + kWarps - 1);
-  const int i_lo = (a.wr < 0) ? 0 : max(0, j0 - a.wr);
-  const int i_hi = (a.wl < 0) ? a.lq : min(a.lq, jlast + a.wl + 1);
+  const int i_lo = (int)max(0LL, (long long)j0 - a.wr);
+  const int i_hi = (int)max((long long)i_lo, min((long long)a.lq, (long long)jlast + a.wl + 1));
   float accK[kMaxD / 32], accV[kMaxD / 32];
 #pragma unroll
   for (int t = 0; t < kMaxD / 32; ++t) accK[t] = accV[t] = 0.f;

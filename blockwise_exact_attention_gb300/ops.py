@@ -73,16 +73,19 @@ def flash_mha_fwd(q, k, v, softmax_scale=None, is_causal=False, window_size=(-1,
 
 
 def flash_mha_fwd_merge(q, k, v, out_acc, lse_acc, softmax_scale=None, is_causal=False, window_size=(-1, -1),
-                        out_final=None):
+                        out_final=None, key_offset=None):
     """Fused ring step: the forward of (q, k, v) folded into the fp32
     accumulator (out_acc, lse_acc) in place by the log-sum-exp merge;
-    ``out_final`` (bf16) also receives the merged rows."""
+    ``out_final`` (bf16) also receives the merged rows. ``key_offset``: the
+    position of key 0 relative to query 0 (default lq - lk)."""
+    if key_offset is None:
+        key_offset = q.shape[1] - k.shape[1]
     lib = _lib.load()
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(q.shape[3])
     ds = [_desc(x) for x in (q, k, v, out_acc, lse_acc, out_final)]
     rc = lib.bea_flash_mha_fwd_merge(*[_ref(x) for x in ds], float(softmax_scale), int(bool(is_causal)),
-                                     int(window_size[0]), int(window_size[1]), _stream())
+                                     int(window_size[0]), int(window_size[1]), int(key_offset), _stream())
     _lib.check(rc, "flash_mha_fwd_merge")
     _count()
     return out_acc, lse_acc
@@ -138,17 +141,20 @@ def flash_mha_bwd_prepare(dout, out, lse, workspace):
 
 
 def flash_mha_bwd_kv_block(dout, q, k, v, dk, dv, softmax_scale=None, is_causal=False, window_size=(-1, -1),
-                           accumulate=False, workspace=None):
+                           accumulate=False, workspace=None, key_offset=None):
     """Stage 2: one K/V block's dK, dV (written or added) and its share of dQ
-    (added into the workspace accumulator)."""
+    (added into the workspace accumulator). ``key_offset``: the position of
+    this block's key 0 relative to query 0 (default lq - lk)."""
+    if key_offset is None:
+        key_offset = q.shape[1] - k.shape[1]
     lib = _lib.load()
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(q.shape[3])
     ds = [_desc(x) for x in (dout, q, k, v, dk, dv)]
     wp, wb = _ws_args(workspace, q)
     rc = lib.bea_flash_mha_bwd_kv_block(*[_ref(x) for x in ds], float(softmax_scale), int(bool(is_causal)),
-                                        int(window_size[0]), int(window_size[1]), int(bool(accumulate)), wp, wb,
-                                        _stream())
+                                        int(window_size[0]), int(window_size[1]), int(key_offset),
+                                        int(bool(accumulate)), wp, wb, _stream())
     _lib.check(rc, "flash_mha_bwd_kv_block")
     _count()
     return dk, dv

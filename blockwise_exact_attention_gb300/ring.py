@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import math
 
+import numpy as np
 import torch
 
 from . import ops
@@ -62,28 +63,54 @@ def _step_view(x, first: int, count: int, c: int, l_dim: int):
     return x.as_strided(size, st, x.storage_offset() + first * c * x.stride(l_dim))
 
 
-def _ring_step_groups(n_chunks: int, is_causal: bool, cast: bool):
-    """Per ring step t, the calls that cover its chunk pairs: (first query chunk, first K/V
-    chunk, number of consecutive chunks, whether this is those query chunks' last step).
-    Step t pairs query chunk i with K/V chunk (i - t) mod C; under a causal mask the
-    wrapped pairs are skipped and query chunk i's last step is t = i, so when the result is
-    cast at the last step that chunk gets a call of its own."""
+def _band_has_keys(c: int, is_causal: bool, window, key_offset: int) -> bool:
+    """Whether any of c query rows sees any of c keys whose key 0 sits at query
+    position key_offset (the window compares positions)."""
+    left, right = int(window[0]), int(window[1])
+    if is_causal:
+        right = 0
+    r = np.arange(c, dtype=np.int64)
+    lo = np.zeros(c, dtype=np.int64) if left < 0 else np.maximum(r - left - key_offset, 0)
+    hi = np.full(c, c - 1, dtype=np.int64) if right < 0 else np.minimum(r + right - key_offset, c - 1)
+    return bool((lo <= hi).any())
+
+
+def _ring_step_groups(n_chunks: int, is_causal: bool, cast: bool, window=(-1, -1), c: int = 1):
+    """Per ring step t, the calls that cover its live chunk pairs: (first query chunk,
+    first K/V chunk, number of consecutive chunks, key offset, whether this is those query
+    chunks' last live step). Step t pairs query chunk i with K/V chunk (i - t) mod C: the
+    pairs with i >= t share the key offset -t*c, the wrapped ones (i < t) (C - t)*c. A run
+    of pairs whose key band is empty is skipped (under a causal mask: every wrapped pair;
+    under a window: the pairs beyond it). When the result is cast at each query chunk's
+    last live step, a run is split where that step changes."""
     C = n_chunks
-    groups = []
+    runs = []  # (t, i0, j0, cnt, koff)
     for t in range(C):
-        if is_causal:
-            if cast:
-                parts = [(t, 0, 1, True)] + ([(t + 1, 1, C - 1 - t, False)] if C - 1 - t > 0 else [])
-            else:
-                parts = [(t, 0, C - t, False)]
-        else:
-            parts = [(t, 0, C - t, t == C - 1)] + ([(0, C - t, t, t == C - 1)] if t > 0 else [])
-        groups.append(parts)
+        for (i0, j0, cnt, koff) in ((t, 0, C - t, -t * c), (0, C - t, t, (C - t) * c)):
+            if cnt > 0 and _band_has_keys(c, is_causal, window, koff):
+                runs.append((t, i0, j0, cnt, koff))
+    last = {}
+    for (t, i0, _j0, cnt, _k) in runs:
+        for i in range(i0, i0 + cnt):
+            last[i] = max(last.get(i, -1), t)
+    groups = [[] for _ in range(C)]
+    for (t, i0, j0, cnt, koff) in runs:
+        if not cast:
+            groups[t].append((i0, j0, cnt, koff, False))
+            continue
+        u = 0
+        while u < cnt:
+            fin = last[i0 + u] == t
+            v = u
+            while v < cnt and (last[i0 + v] == t) == fin:
+                v += 1
+            groups[t].append((i0 + u, j0 + u, v - u, koff, fin))
+            u = v
     return groups
 
 
 def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=True, out_dtype=None,
-                       block_dtype=None, fused=None):
+                       block_dtype=None, fused=None, window_size=(-1, -1)):
     """Forward over ring chunk steps -> (out, lse).
 
     ``out_dtype`` fp32 makes the fp32 accumulator itself the result;
@@ -100,6 +127,9 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
     as one call over a batch of chunk views (ring step t pairs query chunk i
     with K/V chunk i - t): n_chunks launches (plus merges) instead of one per
     chunk pair. Batches larger than 1 run their rows one after another.
+    ``window_size`` (fused steps only) masks every chunk pair by sequence
+    position, with its key chunk placed at its distance from the query chunk;
+    pairs entirely outside the window are skipped.
     """
     n, l, h, d = q.shape
     if l % n_chunks:
@@ -108,6 +138,9 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
         softmax_scale = 1.0 / math.sqrt(d)
     if fused is None:
         fused = q.dtype == torch.bfloat16 and block_dtype is None
+    window_size = tuple(int(x) for x in window_size)
+    if window_size != (-1, -1) and not fused:
+        raise ValueError("a windowed ring runs as fused ring steps (bf16 inputs, no block dtype)")
     out_dtype = out_dtype or q.dtype
     block_dtype = block_dtype or q.dtype
     dev = q.device
@@ -119,19 +152,22 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
     for b in range(n):
         qb, kb, vb = q[b:b + 1], k[b:b + 1], v[b:b + 1]
         accb, outb, lseb = acc[b:b + 1], out[b:b + 1], lse[b:b + 1]
-        for t, parts in enumerate(_ring_step_groups(n_chunks, is_causal, cast)):
-            for (i0, j0, cnt, final) in parts:
+        for t, parts in enumerate(_ring_step_groups(n_chunks, is_causal, cast, window_size, c)):
+            for (i0, j0, cnt, koff, final) in parts:
                 qv, kv_, vv = (_step_view(x_, f, cnt, c, 1) for x_, f in ((qb, i0), (kb, j0), (vb, j0)))
                 av, lv = _step_view(accb, i0, cnt, c, 1), _step_view(lseb, i0, cnt, c, 2)
                 fin = _step_view(outb, i0, cnt, c, 1) if (final and cast) else None
-                causal = is_causal and t == 0
                 if t == 0:
-                    # the first block initialises the accumulator (merge with (0, -inf) is the
-                    # identity); a chunk whose only block this is gets its final output at once
-                    ops.flash_mha_fwd(qv, kv_, vv, softmax_scale, causal, out=fin if fin is not None else av, lse=lv)
+                    # the first block (the diagonal, key offset 0) initialises the accumulator
+                    # (merge with (0, -inf) is the identity); a chunk whose only block this is
+                    # gets its final output at once
+                    ops.flash_mha_fwd(qv, kv_, vv, softmax_scale, is_causal, window_size,
+                                      out=fin if fin is not None else av, lse=lv)
                 elif fused:
-                    ops.flash_mha_fwd_merge(qv, kv_, vv, av, lv, softmax_scale, causal, out_final=fin)
+                    ops.flash_mha_fwd_merge(qv, kv_, vv, av, lv, softmax_scale, is_causal, window_size,
+                                            out_final=fin, key_offset=koff)
                 else:
+                    causal = False  # no window: a live off-diagonal pair sees all its keys
                     blk = torch.empty((cnt, c, h, d), dtype=block_dtype, device=dev)
                     lblk = torch.empty((cnt, h, c), dtype=torch.float32, device=dev)
                     ops.flash_mha_fwd(qv, kv_, vv, softmax_scale, causal, out=blk, lse=lblk)
@@ -139,11 +175,18 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
     return out, lse
 
 
-def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=None, is_causal=True):
-    """Backward over every visible chunk pair -> fp32 (dq, dk, dv)."""
+def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=None, is_causal=True,
+                       window_size=(-1, -1)):
+    """Backward over every live chunk pair -> fp32 (dq, dk, dv).
+
+    ``window_size`` masks each chunk pair by sequence position (key chunk
+    placed at its distance from the query chunk, bf16 inputs only); pairs
+    with no visible key are skipped.
+    """
     n, l, h, d = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
+    window_size = tuple(int(x) for x in window_size)
     dev = q.device
     dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
     dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
@@ -156,23 +199,32 @@ def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=Non
     qs, ks, vs = _chunks(q, n_chunks, 1), _chunks(k, n_chunks, 1), _chunks(v, n_chunks, 1)
     dos, os_, ls = _chunks(dout, n_chunks, 1), _chunks(out, n_chunks, 1), _chunks(lse, n_chunks, 2)
     dqs, dks, dvs = _chunks(dq, n_chunks, 1), _chunks(dk, n_chunks, 1), _chunks(dv, n_chunks, 1)
+    c = l // n_chunks
     staged = q.dtype == torch.bfloat16
-    for i, steps in enumerate(chunk_schedule(n_chunks, is_causal)):
-        live = [(j, kind) for _t, j, kind in steps if kind != "skip"]
+    if window_size != (-1, -1) and not staged:
+        raise ValueError("a windowed ring backward needs bf16 inputs")
+    for i in range(n_chunks):
+        live = []
+        for t in range(n_chunks):
+            j = (i - t) % n_chunks
+            if _band_has_keys(c, is_causal, window_size, (j - i) * c):
+                live.append(j)
         if staged:
             # D of query chunk i once, its dQ summed over every visible K/V chunk in the fp32
             # workspace accumulator, one conversion at the end
             ops.flash_mha_bwd_prepare(dos[i], os_[i], ls[i], ws)
-        for j, kind in live:
+        for j in live:
             # causal, query chunks in ascending order: the diagonal pair (i, i) is the
             # first to touch dk_i and dv_i, so it overwrites instead of adding
-            first = is_causal and kind == "causal"
+            first = is_causal and j == i
             if staged:
                 ops.flash_mha_bwd_kv_block(dos[i], qs[i], ks[j], vs[j], dks[j], dvs[j], softmax_scale,
-                                           kind == "causal", accumulate=not first, workspace=ws)
+                                           is_causal, window_size, accumulate=not first, workspace=ws,
+                                           key_offset=(j - i) * c)
             else:
-                ops.flash_mha_bwd(dos[i], qs[i], ks[j], vs[j], os_[i], ls[i], softmax_scale, kind == "causal",
+                ops.flash_mha_bwd(dos[i], qs[i], ks[j], vs[j], os_[i], ls[i], softmax_scale, is_causal and j == i,
                                   dq=dqs[i], dk=dks[j], dv=dvs[j], accumulate=not first, workspace=ws)
         if staged:
+            # the diagonal pair (key offset 0) always has visible keys, so `live` is never empty
             ops.flash_mha_bwd_finish(dqs[i], softmax_scale, accumulate=False, workspace=ws)
     return dq, dk, dv

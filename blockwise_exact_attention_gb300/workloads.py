@@ -121,7 +121,7 @@ def make_inputs(w: Workload, with_dout: bool = True) -> dict[str, np.ndarray]:
 def small_case(n=1, l=300, h=4, h_kv=2, d=128, is_causal=True, window=(-1, -1),
                dtype="bf16", seed=7, lk=None) -> dict[str, np.ndarray]:
     """Seeded inputs of an arbitrary small shape (ragged tails, odd sizes).
-    ``lk`` (default ``l``) sets the key length for non-causal cases."""
+    ``lk`` (default ``l``) sets the key length."""
     lk = l if lk is None else lk
     rng = np.random.default_rng(seed)
     arrs = {

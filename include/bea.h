@@ -33,7 +33,14 @@
  *   iff (left < 0 || j >= i - left) && (right < 0 || j <= i + right). The
  *   pages only ever pass (-1, -1); this inclusive reading is the library's.
  *   is_causal forces right = 0; right > 0 together with is_causal is an
- *   argument error. Causal or windowed calls need lq == lk.
+ *   argument error.
+ *   Positions: the window compares sequence positions, with key j at position
+ *   j + key_offset relative to query i at position i. bea_flash_mha_fwd and
+ *   bea_flash_mha_bwd use key_offset = lq - lk, which aligns the last query
+ *   with the last key (bottom-right; 0 when lq == lk, the only case the pages
+ *   use); the fused ring step and the K/V-block stage take it explicitly (a
+ *   ring chunk pair passes the distance between its key and query chunks).
+ *   Sequence lengths must be below 2^30.
  *   A query row that sees no key gets out = 0 and lse = -inf.
  *
  * Streams and errors.
@@ -116,6 +123,8 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
  *   lse_acc    [n, h, lq]    f32, read and written
  *   out_final  NULL, or [n, lq, h, d] bf16: also receives the merged rows cast
  *              to bf16 (the last step of a ring)
+ *   key_offset position of key 0 relative to query 0 (see Masks); |key_offset|
+ *              <= 2^30
  * Per row, with La the accumulator's and L the block's log-sum-exp:
  * M = max(La, L); if M == -inf the row is left unchanged; otherwise
  * L' = M + log1p(exp(min(La, L) - M)), out_acc <- exp(La - L') out_acc +
@@ -123,7 +132,7 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
  */
 int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,
                             const bea_tensor* lse_acc, const bea_tensor* out_final, float softmax_scale, int is_causal,
-                            int window_left, int window_right, void* stream);
+                            int window_left, int window_right, int64_t key_offset, void* stream);
 
 /*
  * Bytes of device workspace bea_flash_mha_bwd needs for q of shape
@@ -183,8 +192,9 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
  *          q [n, lq, h, d] bf16, k, v [n, lk, h_kv, d] bf16; dk, dv
  *          [n, lk, h_kv, d] bf16 or f32, written (accumulate 0) or added to
  *          (accumulate 1, both f32). Adds this block's dS k into the
- *          accumulator. The mask arguments are those of bea_flash_mha_bwd and
- *          apply to this (q, k) pair.
+ *          accumulator. The mask arguments are those of bea_flash_mha_bwd,
+ *          with key_offset the position of this block's key 0 relative to
+ *          query 0 (see Masks).
  * finish   dq [n, lq, h, d] bf16 or f32: dq = softmax_scale * accumulator,
  *          written (accumulate 0) or added to an f32 dq (accumulate 1).
  */
@@ -193,7 +203,8 @@ int bea_flash_mha_bwd_prepare(const bea_tensor* dout, const bea_tensor* out, con
 int bea_flash_mha_bwd_kv_block(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k,
                                const bea_tensor* v, const bea_tensor* dk, const bea_tensor* dv,
                                float softmax_scale, int is_causal, int window_left, int window_right,
-                               int accumulate, void* workspace, size_t workspace_bytes, void* stream);
+                               int64_t key_offset, int accumulate, void* workspace, size_t workspace_bytes,
+                               void* stream);
 int bea_flash_mha_bwd_finish(const bea_tensor* dq, float softmax_scale, int accumulate, void* workspace,
                              size_t workspace_bytes, void* stream);
 

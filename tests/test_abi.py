@@ -75,9 +75,11 @@ def test_fwd_rejects_bad_arguments(lib):
     assert fwd(lib, q, k, v, o, l, causal=2) == ARG
     # shapes
     assert fwd(lib, *good(h=4, hkv=3)) == SHAPE
-    q2, k2, v2, o2, l2 = good(l=256, lk=300)
-    assert fwd(lib, q2, k2, v2, o2, l2, causal=1) == SHAPE
-    assert fwd(lib, q2, k2, v2, o2, l2, wl=16) == SHAPE
+    # lq != lk under a mask is valid (bottom-right alignment); lengths of 2^30 or more are not
+    q3, k3, v3, o3, l3 = good(l=1 << 30, lk=300)
+    assert fwd(lib, q3, k3, v3, o3, l3, causal=1) == SHAPE
+    q4, k4, v4, o4, l4 = good(l=256, lk=1 << 30)
+    assert fwd(lib, q4, k4, v4, o4, l4, wl=16) == SHAPE
     assert fwd(lib, q, k, v, o, T([1, 4, 255], F32)) == SHAPE
     assert fwd(lib, q, k, v, T([1, 256, 4], BF16), l) == SHAPE
     assert fwd(lib, q, T([1, 256, 2, 64]), v, o, l) == SHAPE
@@ -145,7 +147,7 @@ def test_staged_bwd_rejects_bad_arguments(lib):
         return lib.bea_flash_mha_bwd_prepare(r(do), r(out), r(lse), ws, wsb, None)
 
     def block(q=q, k=k, dk=dk, dv=dv, acc=1, ws=FAKE, wsb=need, causal=1, wr=-1):
-        return lib.bea_flash_mha_bwd_kv_block(r(do), r(q), r(k), r(v), r(dk), r(dv), 0.125, causal, -1, wr, acc,
+        return lib.bea_flash_mha_bwd_kv_block(r(do), r(q), r(k), r(v), r(dk), r(dv), 0.125, causal, -1, wr, 0, acc,
                                               ws, wsb, None)
 
     def fin(dq=dq, acc=0, ws=FAKE, wsb=need, scale=0.125):
@@ -173,9 +175,9 @@ def test_fwd_merge_rejects_bad_arguments(lib):
     r = ctypes.byref
     acc = T([1, 256, 4, 128], F32)
 
-    def call(q=q, k=k, acc=acc, lse=l, fin=None):
+    def call(q=q, k=k, acc=acc, lse=l, fin=None, off=0):
         return lib.bea_flash_mha_fwd_merge(r(q), r(k), r(v), r(acc), r(lse), r(fin) if fin is not None else None,
-                                           0.125, 1, -1, -1, None)
+                                           0.125, 1, -1, -1, off, None)
 
     assert call(acc=T([1, 256, 4, 128], BF16)) == DTYPE          # the accumulator is fp32
     assert call(acc=T([1, 255, 4, 128], F32)) == SHAPE
@@ -183,6 +185,7 @@ def test_fwd_merge_rejects_bad_arguments(lib):
     assert call(fin=T([1, 256, 4, 128], F32)) == DTYPE           # the final copy is bf16
     assert call(q=T([1, 256, 4, 128], F32), k=T([1, 256, 2, 128], F32)) == DTYPE  # v stays bf16
     assert call(acc=T([1, 256, 4, 128], F32, ptr=FAKE + 4)) == ALIGN
+    assert call(off=(1 << 30) + 1) == ARG                        # key offset out of range
 
 
 def test_merge_rejects_bad_arguments(lib):

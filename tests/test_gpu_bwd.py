@@ -71,6 +71,9 @@ CASES = [
     (1, 640, 8, 2, 64, True, (-1, -1), None),
     (1, 700, 2, 2, 128, True, (0, 0), None),
     (3, 129, 4, 4, 128, True, (-1, -1), None),
+    # lq != lk under a mask: the last query aligned with the last key
+    (1, 200, 2, 1, 64, True, (-1, -1), 333),
+    (1, 300, 2, 2, 128, True, (50, 0), 170),     # the first 130 rows see no key
 ]
 
 

@@ -53,6 +53,10 @@ CASES = [
     (1, 700, 2, 2, 128, True, (0, 0), None),
     (1, 260, 2, 2, 64, False, (-1, 3), None),
     (3, 129, 4, 4, 128, True, (-1, -1), None),
+    # lq != lk under a mask: the last query aligned with the last key
+    (1, 200, 2, 1, 64, True, (-1, -1), 333),
+    (1, 300, 2, 2, 128, True, (50, 0), 170),     # the first 130 rows see no key
+    (1, 129, 4, 2, 128, False, (16, 8), 300),
 ]
 
 

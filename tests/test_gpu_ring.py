@@ -178,3 +178,33 @@ def test_ring_fused_equals_unfused(causal):
     assert_close_bf16(to_np(fo), oo, "fused ring out", output_is_bf16=False)
     assert_close(to_np(fl), ol, TOL_LSE, "fused ring lse")
     assert bea.device_status() == 0
+
+
+# ---- the window-aware ring ------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal,window", [(True, (700, 0)), (False, (300, 200)), (True, (0, 0))])
+def test_ring_windowed(causal, window):
+    """Ring steps masked by sequence position: every live chunk pair gets its key offset,
+    pairs outside the window are skipped; forward and backward against the oracle's windowed
+    ring replay and against the single call."""
+    import blockwise_exact_attention_gb300 as bea
+    x = workloads.small_case(n=1, l=2048, h=4, h_kv=2, d=128, is_causal=causal, window=window, seed=60)
+    scale = 1.0 / math.sqrt(128)
+    q, k, v, do = (to_dev(x[s_], torch.bfloat16) for s_ in ("q", "k", "v", "dout"))
+    ro, rl = bea.ring_attention_fwd(q, k, v, 8, scale, causal, out_dtype=torch.float32, window_size=window)
+    so, sl = bea.flash_mha_fwd(q, k, v, scale, causal, window, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    oo, ol = oracle.ring_fwd_replay(x["q"], x["k"], x["v"], scale, 8, causal, window)
+    assert_close_bf16(to_np(ro), oo, "windowed ring out", output_is_bf16=False)
+    assert_close(to_np(rl), ol, TOL_LSE, "windowed ring lse")
+    assert_close_bf16(to_np(ro), to_np(so).astype(np.float64), "windowed ring vs single", output_is_bf16=False)
+    # backward from the oracle's out/lse, against the oracle's windowed ring backward
+    o_up = workloads.round_to_bf16(oo.astype(np.float32))
+    l_up = ol.astype(np.float32)
+    o, lse = to_dev(o_up, torch.bfloat16), to_dev(l_up, torch.float32)
+    rg = bea.ring_attention_bwd(do, q, k, v, o, lse, 8, scale, causal, window)
+    torch.cuda.synchronize()
+    ref = oracle.ring_bwd_replay(x["dout"], x["q"], x["k"], x["v"], o_up, l_up, scale, 8, causal, window)
+    for name, a, r in zip(("dq", "dk", "dv"), rg, ref):
+        assert_close_bf16(to_np(a), r, name, output_is_bf16=False)
+    assert bea.device_status() == 0
