@@ -149,6 +149,26 @@ def attention_flops(n, h, lq, lk, d, is_causal, window=(-1, -1)):
 
 
 # ---------------------------------------------------------------------------
+# replicas: the slowest rank sets the pace
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum over ranks of per-rank timings (identity with one
+    rank or without an initialised process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: the work of every replica over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle legs (the reference arm and the cpu_baseline field)
 # ---------------------------------------------------------------------------
 
@@ -343,11 +363,8 @@ def main():
     ms_bwd = sum(t_bwd) / len(t_bwd)
     ms_main = sum(t_main) / len(t_main)
     ms_step = ms_fwd + ms_bwd
-    if dist:
-        tt = torch.tensor([ms_step, ms_fwd, ms_bwd, ms_main], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd, ms_bwd, ms_main = (float(v_) for v_ in tt)
-    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    ms_step, ms_fwd, ms_bwd, ms_main = max_over_ranks([ms_step, ms_fwd, ms_bwd, ms_main], dist, dev)
+    value = job_tflops(world, f_fwd + f_bwd, ms_step)
     fwd_tf = f_fwd / (ms_fwd * 1e-3) / 1e12
     bwd_tf = f_bwd / (ms_bwd * 1e-3) / 1e12
     main_tf = f_bwd / (ms_main * 1e-3) / 1e12
@@ -374,11 +391,8 @@ def main():
         h_dv.copy_(dv, non_blocking=True)
 
     e2e_ms = statistics.mean(timed(e2e_step, max(3, args.steps // 4), 2))
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt[0])
-    e2e_val = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
+    e2e_val = job_tflops(world, f_fwd + f_bwd, e2e_ms)
 
     # ---- ring_merge standalone, [1, 16384, 16, 128], L2 flushed ----
     wr = workloads.WORKLOADS["ring_causal_16k"]
