@@ -377,18 +377,32 @@ def main():
     h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hdo_))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_dq, h_dk, h_dv))
 
+    copy_stream = torch.cuda.Stream(device=dev)
+
     def e2e_step():
+        # q, k, v go up on the compute stream; dout goes up on a second stream while the
+        # forward runs, and out/lse come down there while the backward runs. The step
+        # ends on the compute stream once every copy has landed.
+        copy_stream.wait_stream(stream)          # the previous step is done with dout and out
         q.copy_(hq_, non_blocking=True)
         k.copy_(hk_, non_blocking=True)
         v.copy_(hv_, non_blocking=True)
-        do.copy_(hdo_, non_blocking=True)
+        with torch.cuda.stream(copy_stream):
+            do.copy_(hdo_, non_blocking=True)
+            do_ready = copy_stream.record_event()
         fwd()
+        fwd_done = stream.record_event()
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(fwd_done)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            outs_down = copy_stream.record_event()
+        stream.wait_event(do_ready)
         bwd()
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
         h_dq.copy_(dq, non_blocking=True)
         h_dk.copy_(dk, non_blocking=True)
         h_dv.copy_(dv, non_blocking=True)
+        stream.wait_event(outs_down)
 
     e2e_ms = statistics.mean(timed(e2e_step, max(3, args.steps // 4), 2))
     e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
