@@ -63,9 +63,10 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """nvidia-smi clock/throttle samples every 10 ms; the summary keeps the
+    samples taken between mark_start() and mark_end() (the timed region)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -73,12 +74,19 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = os.path.join("/tmp", f"bea_clocks_{os.getpid()}.csv")
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __enter__(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -97,23 +105,27 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]),
+                             {nm for nm, val in zip(names, parts[5:9]) if val.lower().startswith("active")}))
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(nm)
-        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 - 0.02 <= r[0] <= self.t1 + 0.02]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["no samples"]}
+        reasons = set().union(*(r[3] for r in use))
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": use[-1][2],
+                "samples": len(use), "samples_in_timed_region": len(inside), "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -344,6 +356,7 @@ def main():
     t_fwd, t_bwd, t_main = [], [], []
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
+        clk.mark_start()
         for _ in range(args.steps):
             flush_l2()
             e0, e1, e2, m0, m1 = (torch.cuda.Event(enable_timing=True) for _ in range(5))
@@ -357,6 +370,7 @@ def main():
             t_bwd.append(e1.elapsed_time(e2))
             t_main.append(m0.elapsed_time(m1))
         torch.cuda.synchronize()
+        clk.mark_end()
     launches = bea.launches_since_reset(reset=True)
     status = bea.device_status()
     ms_fwd = sum(t_fwd) / len(t_fwd)
