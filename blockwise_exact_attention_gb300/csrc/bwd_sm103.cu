@@ -91,99 +91,143 @@ struct BwdCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Row `i` of query head `hq` in the fp32 dQ accumulator ([n, h, lq_pad, d], row-major).
-__device__ __forceinline__ float* dq_acc_row(const BwdParams& p, int b, int hq, int i) {
-  return p.dq_acc + ((size_t)(b * p.a.h + hq) * p.lq_pad + i) * p.a.d;
+// The fp32 dQ accumulator is [n, h, lq_pad, d], row-major.
+
+// ---------------------------------------------------------------------------
+// 1. preprocess and 3. convert: HBM-bound row kernels
+// ---------------------------------------------------------------------------
+//
+// A group of D/8 threads owns a row, each thread 8 consecutive elements
+// (16-byte loads and stores); every thread keeps two rows in flight and the
+// grid is one wave of resident CTAs.
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 raw, float* f) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
+    f[2 * u] = t.x;
+    f[2 * u + 1] = t.y;
+  }
 }
 
-// ---------------------------------------------------------------------------
-// 1. preprocess
-// ---------------------------------------------------------------------------
+// Eight elements of row i of a [n, l, h, d] tensor starting at column c, as fp32.
+__device__ __forceinline__ void load8(const Seq4& t, bool f32, int b, int i, int hh, int c, float* f) {
+  if (f32) {
+    const float* src = reinterpret_cast<const float*>(t.ptr) + b * t.sn + (int64_t)i * t.sl + hh * t.sh + c;
+    const float4 lo = *reinterpret_cast<const float4*>(src);
+    const float4 hi = *reinterpret_cast<const float4*>(src + 4);
+    f[0] = lo.x; f[1] = lo.y; f[2] = lo.z; f[3] = lo.w;
+    f[4] = hi.x; f[5] = hi.y; f[6] = hi.z; f[7] = hi.w;
+  } else {
+    const __nv_bfloat16* src =
+        reinterpret_cast<const __nv_bfloat16*>(t.ptr) + b * t.sn + (int64_t)i * t.sl + hh * t.sh + c;
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(src), f);
+  }
+}
 
-__global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdParams p) {
+// D = rowsum(dO * O), L * log2(e) (+inf for rows without keys and for padding
+// rows, so that their P is exactly 0) and a zeroed row of the dQ accumulator,
+// for every padded query row.
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) bwd_preprocess_kernel(BwdParams p) {
+  constexpr int kTpr = D / 8;
+  constexpr int kRowsPerPass = kRowThreads / kTpr;
   const AttnDims& a = p.a;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // over n * h * lq_pad
   const int64_t total = (int64_t)a.n * a.h * p.lq_pad;
-  if (row >= total) return;
-  const int i = (int)(row % p.lq_pad);
-  const int bh = (int)(row / p.lq_pad);
-  const int hq = bh % a.h, b = bh / a.h;
-  float dsum = 0.f, l2 = INFINITY;
-  if (i < a.lq) {
-    const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout.ptr) + b * p.dout.sn +
-                             (int64_t)i * p.dout.sl + hq * p.dout.sh;
-    for (int c = lane * 4; c < a.d; c += 128) {
-      const uint2 graw = *reinterpret_cast<const uint2*>(g + c);
-      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
-      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
-      float4 o;
-      if (p.out_is_f32) {
-        o = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out.ptr) + b * p.out.sn +
-                                             (int64_t)i * p.out.sl + hq * p.out.sh + c);
-      } else {
-        const uint2 oraw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.out.ptr) +
-                                                           b * p.out.sn + (int64_t)i * p.out.sl + hq * p.out.sh + c);
-        const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&oraw.x));
-        const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&oraw.y));
-        o = make_float4(o01.x, o01.y, o23.x, o23.y);
+  const int sub = threadIdx.x / kTpr;
+  const int c = (threadIdx.x % kTpr) * 8;
+  const unsigned lane0 = (threadIdx.x & 31u) / kTpr * kTpr;
+  const unsigned group_mask = (kTpr >= 32) ? 0xffffffffu : (((1u << kTpr) - 1u) << lane0);
+  const int64_t stride = (int64_t)gridDim.x * kRowsPerPass * 2;
+  for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerPass * 2 + sub; r0 < total; r0 += stride) {
+    float dsum[2] = {0.f, 0.f}, lse[2] = {-INFINITY, -INFINITY};
+    int64_t rows[2] = {r0, r0 + kRowsPerPass};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t row = rows[u];
+      if (row >= total) continue;
+      const int i = (int)(row % p.lq_pad);
+      const int bh = (int)(row / p.lq_pad);
+      const int hq = bh % a.h, b = bh / a.h;
+      if (i < a.lq) {
+        float g[8], o[8];
+        load8(p.dout, false, b, i, hq, c, g);
+        load8(p.out, p.out_is_f32 != 0, b, i, hq, c, o);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dsum[u] = fmaf(g[e], o[e], dsum[u]);
+        lse[u] = p.lse.ptr[b * p.lse.sn + hq * p.lse.sh + i];
       }
-      dsum = fmaf(g01.x, o.x, dsum);
-      dsum = fmaf(g01.y, o.y, dsum);
-      dsum = fmaf(g23.x, o.z, dsum);
-      dsum = fmaf(g23.y, o.w, dsum);
+      float* acc = p.dq_acc + (size_t)row * D + c;
+      *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(acc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-    const float L = p.lse.ptr[b * p.lse.sn + hq * p.lse.sh + i];
-    if (L != -INFINITY) l2 = L * 1.4426950408889634f;
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int off = kTpr / 2; off > 0; off >>= 1) dsum[u] += __shfl_xor_sync(group_mask, dsum[u], off);
+      if (c == 0 && rows[u] < total) {
+        p.d_row[rows[u]] = dsum[u];
+        p.lse2[rows[u]] = (lse[u] == -INFINITY) ? INFINITY : lse[u] * 1.4426950408889634f;
+      }
+    }
   }
-  if (lane == 0) {
-    p.d_row[row] = (i < a.lq) ? dsum : 0.f;
-    p.lse2[row] = l2;
-  }
-  // zero this row of the dQ accumulator
-  float* acc = dq_acc_row(p, b, hq, i);
-  for (int c = lane * 4; c < a.d; c += 128) *reinterpret_cast<float4*>(acc + c) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// ---------------------------------------------------------------------------
-// 3. convert
-// ---------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(256) bwd_convert_dq_kernel(BwdParams p) {
+// dq = scale * accumulator, cast to bf16, written, or added to an fp32 dq.
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) bwd_convert_dq_kernel(BwdParams p) {
+  constexpr int kTpr = D / 8;
+  constexpr int kRowsPerPass = kRowThreads / kTpr;
   const AttnDims& a = p.a;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // over n * h * lq
   const int64_t total = (int64_t)a.n * a.h * a.lq;
-  if (row >= total) return;
-  const int i = (int)(row % a.lq);
-  const int bh = (int)(row / a.lq);
-  const int hq = bh % a.h, b = bh / a.h;
-  const float* acc = dq_acc_row(p, b, hq, i);
-  for (int c = lane * 4; c < a.d; c += 128) {
-    float4 v = *reinterpret_cast<const float4*>(acc + c);
-    v.x *= a.scale;
-    v.y *= a.scale;
-    v.z *= a.scale;
-    v.w *= a.scale;
-    if (p.dq_is_f32) {
-      float* dst = reinterpret_cast<float*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
-      if (p.accumulate) {
-        const float4 o = *reinterpret_cast<const float4*>(dst);
-        v.x += o.x;
-        v.y += o.y;
-        v.z += o.z;
-        v.w += o.w;
+  const int sub = threadIdx.x / kTpr;
+  const int c = (threadIdx.x % kTpr) * 8;
+  const int64_t stride = (int64_t)gridDim.x * kRowsPerPass * 2;
+  for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerPass * 2 + sub; r0 < total; r0 += stride) {
+    float v[2][8];
+    int64_t rows[2] = {r0, r0 + kRowsPerPass};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (rows[u] >= total) continue;
+      const int i = (int)(rows[u] % a.lq);
+      const int bh = (int)(rows[u] / a.lq);
+      const float* acc = p.dq_acc + ((size_t)bh * p.lq_pad + i) * D + c;
+      const float4 lo = *reinterpret_cast<const float4*>(acc);
+      const float4 hi = *reinterpret_cast<const float4*>(acc + 4);
+      v[u][0] = lo.x; v[u][1] = lo.y; v[u][2] = lo.z; v[u][3] = lo.w;
+      v[u][4] = hi.x; v[u][5] = hi.y; v[u][6] = hi.z; v[u][7] = hi.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (rows[u] >= total) continue;
+      const int i = (int)(rows[u] % a.lq);
+      const int bh = (int)(rows[u] / a.lq);
+      const int hq = bh % a.h, b = bh / a.h;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[u][e] *= a.scale;
+      if (p.dq_is_f32) {
+        float* dst = reinterpret_cast<float*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
+        if (p.accumulate) {
+          const float4 lo = *reinterpret_cast<const float4*>(dst);
+          const float4 hi = *reinterpret_cast<const float4*>(dst + 4);
+          v[u][0] += lo.x; v[u][1] += lo.y; v[u][2] += lo.z; v[u][3] += lo.w;
+          v[u][4] += hi.x; v[u][5] += hi.y; v[u][6] += hi.z; v[u][7] += hi.w;
+        }
+        *reinterpret_cast<float4*>(dst) = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+      } else {
+        __nv_bfloat16* dst =
+            reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
+        uint4 raw;
+        raw.x = pack_bf16x2(v[u][0], v[u][1]);
+        raw.y = pack_bf16x2(v[u][2], v[u][3]);
+        raw.z = pack_bf16x2(v[u][4], v[u][5]);
+        raw.w = pack_bf16x2(v[u][6], v[u][7]);
+        *reinterpret_cast<uint4*>(dst) = raw;
       }
-      *reinterpret_cast<float4*>(dst) = v;
-    } else {
-      __nv_bfloat16* dst =
-          reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
-      uint2 raw;
-      raw.x = pack_bf16x2(v.x, v.y);
-      raw.y = pack_bf16x2(v.z, v.w);
-      *reinterpret_cast<uint2*>(dst) = raw;
     }
   }
 }
@@ -638,10 +682,29 @@ cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const C
 
 }  // namespace
 
+// One wave of resident CTAs of a row kernel over `rows` rows of D values.
+template <typename K>
+cudaError_t row_grid(K kern, int64_t rows, int d, unsigned* grid) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, 0)) != cudaSuccess) return e;
+  const int64_t rows_per_block = (int64_t)kRowThreads / (d / 8) * 2;
+  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  *grid = (unsigned)(blocks < cap ? blocks : cap);
+  return cudaSuccess;
+}
+
 cudaError_t launch_bwd_prepare(const BwdParams& p, cudaStream_t s, int* nlaunch) {
   const int64_t rows = (int64_t)p.a.n * p.a.h * p.lq_pad;
   if (rows == 0) return cudaSuccess;
-  bwd_preprocess_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+  auto kern = (p.a.d == 128) ? bwd_preprocess_kernel<128> : bwd_preprocess_kernel<64>;
+  unsigned grid = 0;
+  cudaError_t e = row_grid(kern, rows, p.a.d, &grid);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kRowThreads, 0, s>>>(p);
   *nlaunch += 1;
   return cudaGetLastError();
 }
@@ -656,7 +719,11 @@ cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUt
 cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch) {
   const int64_t qrows = (int64_t)p.a.n * p.a.h * p.a.lq;
   if (qrows == 0) return cudaSuccess;
-  bwd_convert_dq_kernel<<<(unsigned)((qrows + 7) / 8), 256, 0, s>>>(p);
+  auto kern = (p.a.d == 128) ? bwd_convert_dq_kernel<128> : bwd_convert_dq_kernel<64>;
+  unsigned grid = 0;
+  cudaError_t e = row_grid(kern, qrows, p.a.d, &grid);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kRowThreads, 0, s>>>(p);
   *nlaunch += 1;
   return cudaGetLastError();
 }
