@@ -358,13 +358,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // softmax_scale > 0, so the max commutes with the scaling. Eight
-      // independent partial maxima keep the dependent chain short.
+      // independent partial maxima keep the dependent chain short; the
+      // three-input max takes two new values per instruction.
+      // Partial maximum u covers columns u + 8k, k = 0..15.
       float m8[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(sr[c]);
+      for (int u = 0; u < 8; ++u) {
+        float m = fmax3(__uint_as_float(sr[u]), __uint_as_float(sr[u + 8]), __uint_as_float(sr[u + 16]));
 #pragma unroll
-      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int k = 3; k < 15; k += 2) m = fmax3(m, __uint_as_float(sr[u + 8 * k]), __uint_as_float(sr[u + 8 * k + 8]));
+        m8[u] = fmaxf(m, __uint_as_float(sr[u + 120]));
+      }
+      float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       mx *= scale_log2;
       const float m_new = fmaxf(m_ref, mx);
       const bool grow = m_new > m_ref + kRescaleThreshold;  // also true when m_ref = -inf, m_new finite
