@@ -51,6 +51,18 @@ constexpr int kProducerWarp = 8;  // Q and K loads
 constexpr int kMmaWarp = 9;
 constexpr int kVLoadWarp = 10;    // V loads
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// "P_t of tile j is in TMEM" goes from softmax warpgroup t to the MMA warp over
+// hardware named barrier kPReadyBar + t: one phase per tile, 128 softmax threads
+// plus the MMA warp. A named barrier has no time limit, so the phases are kept
+// matched on every path:
+//  * the MMA warp joins once per tile of subtile t; after an abort it still
+//    joins, without work, for each tile it has not reached;
+//  * each softmax warp joins once per tile of its range. On the normal path it
+//    arrives without waiting: it cannot reach tile j+1 before S_t(j+1), which
+//    the MMA warp issues only after phase j. After an abort it joins with a
+//    waiting sync, so that it never runs a phase ahead of the MMA warp.
+constexpr uint32_t kPReadyBar = 1;
+constexpr uint32_t kPReadyThreads = 128 + 32;
 
 template <int D>
 struct FwdCfg {
@@ -61,7 +73,7 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + kSub * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kSub + 1;
+  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
@@ -109,8 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = v_full + C::kStages;  // K and V rings are released separately:
   uint64_t* v_empty = k_empty + C::kStages; // K_j after the S of tile j, V_j after its P V
   uint64_t* s_full = v_empty + C::kStages;
-  uint64_t* p_full = s_full + kSub;
-  uint64_t* o_full = p_full + kSub;
+  uint64_t* o_full = s_full + kSub;
   uint64_t* mma_done = o_full + kSub;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -151,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < kSub; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], kBlockM);
       mbar_init(&o_full[t], 1);
     }
     mbar_init(mma_done, 1);
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool k_next_ready = false;
           if (!(ok = warp_wait_parity(&v_full[s], par, abort_flag, p.status))) break;
           if (a0) {
-            if (!(ok = warp_wait_parity(&p_full[0], pv0 & 1, abort_flag, p.status))) break;
+            named_bar_sync(kPReadyBar + 0, kPReadyThreads);  // P_0 of tile j is in TMEM
             tc_fence_after();
             BEA_ISSUE_PV(0, s, pv0 == 0);
             ++pv0;
@@ -297,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             BEA_ISSUE_S(0, s1);
           }
           if (a1) {
-            if (!(ok = warp_wait_parity(&p_full[1], pv1 & 1, abort_flag, p.status))) break;
+            named_bar_sync(kPReadyBar + 1, kPReadyThreads);  // P_1 of tile j is in TMEM
             tc_fence_after();
             BEA_ISSUE_PV(1, s, pv1 == 0);
             ++pv1;
@@ -317,6 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #undef BEA_ISSUE_S
 #undef BEA_ISSUE_PV
+      // After an abort, join the P-ready phases of the tiles not reached (a no-op otherwise).
+      for (; pv0 < hi0 - lo0; ++pv0) named_bar_sync(kPReadyBar + 0, kPReadyThreads);
+      for (; pv1 < hi1 - lo1; ++pv1) named_bar_sync(kPReadyBar + 1, kPReadyThreads);
       // Everything issued must finish before TMEM is released.
       umma_commit_warp(mma_done);
       volatile int no_abort = 0;
@@ -340,7 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     const int my_lo = t ? sc.lo[1] : sc.lo[0], my_hi = t ? sc.hi[1] : sc.hi[0];  // no dynamic indexing
     for (int j = my_lo; j < my_hi; ++j, ++it) {
-      if (!(ok = warp_wait_parity(&s_full[t], it & 1, abort_flag, p.status))) break;
+      if (ok) ok = warp_wait_parity(&s_full[t], it & 1, abort_flag, p.status);
+      if (!ok) {
+        named_bar_sync(kPReadyBar + t, kPReadyThreads);  // aborted: keep the P-ready phases matched
+        continue;
+      }
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld32(s_tmem + 0, sr);
@@ -413,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      named_bar_arrive(kPReadyBar + t, kPReadyThreads);
     }
     // ---- epilogue ----
     const bool have_o = my_lo < my_hi;

@@ -373,9 +373,19 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Named barrier among `nthreads` threads (a multiple of 32) of the CTA. The
-// warp is reconverged first and the non-.aligned form is used, so a caller
-// whose lane 0 just left a lane-0-only branch is still well defined.
+// ---------------------------------------------------------------------------
+// named (hardware) barriers
+// ---------------------------------------------------------------------------
+
+// Arrive on named barrier `id` without waiting; `nthreads` (a multiple of 32)
+// is the barrier's total participant count.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Arrive on named barrier `id` and wait for `nthreads` arrivals. The warp is
+// reconverged first. A named barrier has no time limit: every use pairs it
+// with producers that arrive on every path, aborts included.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   __syncwarp();
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
