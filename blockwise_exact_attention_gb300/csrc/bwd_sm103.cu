@@ -463,12 +463,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                        k > 0 ? 1u : 0u);
         }
       };
+      // dQ_h^T = K^T dS_h^T (A = K read MN-major, B = dS_h^T from shared memory, MN-major)
+      // into the second half of slot h.
+      auto issue_dq = [&](int h) {
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048),
+                       C::kIdescQ, k > 0 ? 1u : 0u);
+      };
       // dV += P_h^T dO_h (A = P_h^T from TMEM, B = dO MN-major); dK += dS_h^T Q_h (A = dS_h^T
-      // from TMEM, B = Q MN-major); dQ_h^T = K^T dS_h^T (A = K read MN-major, B = dS_h^T from
-      // shared memory, MN-major) into the second half of slot h. Query step k (16 queries)
-      // of the half was formed by key warpgroup k / 2, whose P^T / dS^T columns are
-      // [128h + 32 (k / 2), +16) / [128h + 32 (k / 2) + 16, +16).
-      auto issue_grads = [&](int h, int st, bool first) {
+      // from TMEM, B = Q MN-major). Query step k (16 queries) of the half was formed by key
+      // warpgroup k / 2, whose P^T / dS^T columns are [128h + 32 (k / 2), +16) /
+      // [128h + 32 (k / 2) + 16, +16).
+      auto issue_dkv = [&](int h, int st, bool first) {
         const uint64_t q_mn = sdesc_add(q_mn0, st * C::kTileBytes);
         const uint64_t do_mn = sdesc_add(do_mn0, st * C::kTileBytes);
 #pragma unroll
@@ -479,15 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k)
           umma_ts_warp(tmem + T_DK, tmem + 128u * h + 32 * (k / 2) + 16 + 8 * (k % 2),
                        sdesc_add(q_mn, (4 * h + k) * 2048), C::kIdescKV, (!first || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048),
-                       C::kIdescQ, k > 0 ? 1u : 0u);
       };
       // Issue order: S_0 dP_0 S_1 dP_1 (tile 0), then per tile i
-      //   [P_0/dS_0 ready] grads_0(i), S_0 dP_0 (tile i+1)
-      //   [P_1/dS_1 ready] grads_1(i), S_1 dP_1 (tile i+1)
-      // Slot 0 is free for tile i+1 once grads_0(i) is issued and its dQ_0^T drained, so the
+      //   [P_0/dS_0 ready] dQ_0^T, dV, dK (i), S_0 dP_0 (tile i+1)
+      //   [P_1/dS_1 ready] dQ_1^T, dV, dK (i), S_1 dP_1 (tile i+1)
+      // dQ_h^T goes first, so that the drain reads it out of slot h while dV, dK and S_h run:
+      // dP_h of the next tile waits for that read.
+      // Slot 0 is free for tile i+1 once dV, dK (i) are issued and its dQ_0^T drained, so the
       // key warps' work on each half hides behind the tensor work of the other half.
       bool ok = sc.n_iter > 0 && warp_wait_parity(kv_full, 0, abort_flag, p.status);
       if (ok) ok = warp_wait_parity(&q_full[0], 0, abort_flag, p.status);
@@ -511,8 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(kReadyBar + h, kReadyThreads);  // P_h^T / dS_h^T of tile it are written
           ++n_ready;
           tc_fence_after();
-          issue_grads(h, s, it == 0 && h == 0);
+          issue_dq(h);
           umma_commit_warp(&dq_full[h]);
+          issue_dkv(h, s, it == 0 && h == 0);
           if (h == 1) umma_commit_warp(&qdo_empty[s]);  // the last readers of stage s are issued
           if (more) {
             if (h == 0 && !(ok = warp_wait_parity(&q_full[s1], par1, abort_flag, p.status))) break;
