@@ -404,15 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       uint32_t pk[64];
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      // exponent arguments and the row sum on packed fp32 pairs; eight independent partial sums
+      const uint64_t sl2 = f2(scale_log2, scale_log2), nm2 = f2(neg_m, neg_m);
+      uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, neg_m));
-        ps[c & 7] += p0 + p1;
+        const uint64_t x = f2_fma(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2, nm2);
+        const float p0 = ex2_approx(f2_lo(x));
+        const float p1 = ex2_approx(f2_hi(x));
+        ps[c & 3] = f2_add(ps[c & 3], f2(p0, p1));
         pk[c] = pack_bf16x2(p0, p1);
       }
-      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      const uint64_t s2 = f2_add(f2_add(ps[0], ps[1]), f2_add(ps[2], ps[3]));
+      l_sum += f2_lo(s2) + f2_hi(s2);
       tmem_st32(s_tmem + 0, pk);
       tmem_st32(s_tmem + 32, pk + 32);
       if (rescale) {
