@@ -274,29 +274,29 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t* sv, const uint32_t* pv
                                           int cc, const AttnDims& a, int kj, int q0, float scale_log2,
                                           uint32_t p_dst, uint8_t* ds_row, int j) {
   uint32_t pk[16], dk[16];
+  const uint64_t sl2 = f2(scale_log2, scale_log2);
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
     const float4 L4 = *reinterpret_cast<const float4*>(l2s + cc * 32 + e4 * 4);
     const float4 D4 = *reinterpret_cast<const float4*>(dds + cc * 32 + e4 * 4);
-    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
-    const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-    float pr[4], dsr[4];
+    const uint64_t nL[2] = {f2(-L4.x, -L4.y), f2(-L4.z, -L4.w)};
+    const uint64_t nD[2] = {f2(-D4.x, -D4.y), f2(-D4.z, -D4.w)};
+    // two queries per packed fp32 operation: P = exp2(S scale log2e - L log2e), dS = P (dP - D)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e4 * 4 + u;
-      float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, -Lv[u]));
+    for (int u2 = 0; u2 < 2; ++u2) {
+      const int e = e4 * 4 + 2 * u2;
+      const uint64_t x = f2_fma(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2, nL[u2]);
+      float p0 = ex2_approx(f2_lo(x));
+      float p1 = ex2_approx(f2_hi(x));
       if constexpr (kMask) {
         const int qi = q0 + cc * 32 + e;
-        const bool vis = (kj < a.lk) & key_visible(qi, kj, a.wl, a.wr);
-        pe = vis ? pe : 0.f;
+        p0 = ((kj < a.lk) & key_visible(qi, kj, a.wl, a.wr)) ? p0 : 0.f;
+        p1 = ((kj < a.lk) & key_visible(qi + 1, kj, a.wl, a.wr)) ? p1 : 0.f;
       }
-      pr[u] = pe;
-      dsr[u] = pe * (__uint_as_float(pv[e]) - Dv[u]);
+      const uint64_t ds = f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), nD[u2]));
+      pk[e4 * 2 + u2] = pack_bf16x2(p0, p1);
+      dk[e4 * 2 + u2] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
     }
-    pk[e4 * 2] = pack_bf16x2(pr[0], pr[1]);
-    pk[e4 * 2 + 1] = pack_bf16x2(pr[2], pr[3]);
-    dk[e4 * 2] = pack_bf16x2(dsr[0], dsr[1]);
-    dk[e4 * 2 + 1] = pack_bf16x2(dsr[2], dsr[3]);
   }
   // P^T and dS^T (packed bf16 pairs) over the 32 S^T columns this thread has just read:
   // P^T in the first 16, dS^T in the last 16 (the A operands of dV += P^T dO and dK += dS^T Q)
