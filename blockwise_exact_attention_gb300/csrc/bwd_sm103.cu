@@ -191,56 +191,53 @@ __global__ void __launch_bounds__(kRowThreads) bwd_preprocess_kernel(BwdParams p
   }
 }
 
-// dq = scale * accumulator, cast to bf16, written, or added to an fp32 dq.
+// dq = scale * accumulator, cast to bf16, written, or added to an fp32 dq. The
+// accumulator is [n h][lq_pad / 4][D][4] (four query rows interleaved per
+// head-dim index); a thread takes 8 head-dim entries of a group of four rows:
+// 128 contiguous bytes in, four 8-entry row pieces out.
 template <int D>
 __global__ void __launch_bounds__(kRowThreads) bwd_convert_dq_kernel(BwdParams p) {
-  constexpr int kTpr = D / 8;
-  constexpr int kRowsPerPass = kRowThreads / kTpr;
+  constexpr int kTpg = D / 8;
+  constexpr int kGroupsPerPass = kRowThreads / kTpg;
   const AttnDims& a = p.a;
-  const int64_t total = (int64_t)a.n * a.h * a.lq;
-  const int sub = threadIdx.x / kTpr;
-  const int c = (threadIdx.x % kTpr) * 8;
-  const int64_t stride = (int64_t)gridDim.x * kRowsPerPass * 2;
-  for (int64_t r0 = (int64_t)blockIdx.x * kRowsPerPass * 2 + sub; r0 < total; r0 += stride) {
-    float v[2][8];
-    int64_t rows[2] = {r0, r0 + kRowsPerPass};
+  const int64_t groups_bh = (a.lq + 3) / 4;
+  const int64_t total = (int64_t)a.n * a.h * groups_bh;
+  const int sub = threadIdx.x / kTpg;
+  const int c = (threadIdx.x % kTpg) * 8;
+  const int64_t stride = (int64_t)gridDim.x * kGroupsPerPass;
+  for (int64_t g0 = (int64_t)blockIdx.x * kGroupsPerPass + sub; g0 < total; g0 += stride) {
+    const int64_t bh = g0 / groups_bh;
+    const int gi = (int)(g0 % groups_bh);
+    const float* acc = p.dq_acc + (((size_t)bh * (p.lq_pad / 4) + gi) * D + c) * 4;
+    float4 q4[8];  // q4[k]: the four rows at head-dim entry c + k
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (rows[u] >= total) continue;
-      const int i = (int)(rows[u] % a.lq);
-      const int bh = (int)(rows[u] / a.lq);
-      const float* acc = p.dq_acc + ((size_t)bh * p.lq_pad + i) * D + c;
-      const float4 lo = *reinterpret_cast<const float4*>(acc);
-      const float4 hi = *reinterpret_cast<const float4*>(acc + 4);
-      v[u][0] = lo.x; v[u][1] = lo.y; v[u][2] = lo.z; v[u][3] = lo.w;
-      v[u][4] = hi.x; v[u][5] = hi.y; v[u][6] = hi.z; v[u][7] = hi.w;
-    }
+    for (int k = 0; k < 8; ++k) q4[k] = *reinterpret_cast<const float4*>(acc + 4 * k);
+    const int hq = (int)(bh % a.h), b = (int)(bh / a.h);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (rows[u] >= total) continue;
-      const int i = (int)(rows[u] % a.lq);
-      const int bh = (int)(rows[u] / a.lq);
-      const int hq = bh % a.h, b = bh / a.h;
+    for (int r = 0; r < 4; ++r) {
+      const int i = 4 * gi + r;
+      if (i >= a.lq) break;
+      float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[u][e] *= a.scale;
+      for (int k = 0; k < 8; ++k) v[k] = (r == 0 ? q4[k].x : r == 1 ? q4[k].y : r == 2 ? q4[k].z : q4[k].w) * a.scale;
       if (p.dq_is_f32) {
         float* dst = reinterpret_cast<float*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
         if (p.accumulate) {
           const float4 lo = *reinterpret_cast<const float4*>(dst);
           const float4 hi = *reinterpret_cast<const float4*>(dst + 4);
-          v[u][0] += lo.x; v[u][1] += lo.y; v[u][2] += lo.z; v[u][3] += lo.w;
-          v[u][4] += hi.x; v[u][5] += hi.y; v[u][6] += hi.z; v[u][7] += hi.w;
+          v[0] += lo.x; v[1] += lo.y; v[2] += lo.z; v[3] += lo.w;
+          v[4] += hi.x; v[5] += hi.y; v[6] += hi.z; v[7] += hi.w;
         }
-        *reinterpret_cast<float4*>(dst) = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
       } else {
         __nv_bfloat16* dst =
             reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
         uint4 raw;
-        raw.x = pack_bf16x2(v[u][0], v[u][1]);
-        raw.y = pack_bf16x2(v[u][2], v[u][3]);
-        raw.z = pack_bf16x2(v[u][4], v[u][5]);
-        raw.w = pack_bf16x2(v[u][6], v[u][7]);
+        raw.x = pack_bf16x2(v[0], v[1]);
+        raw.y = pack_bf16x2(v[2], v[3]);
+        raw.z = pack_bf16x2(v[4], v[5]);
+        raw.w = pack_bf16x2(v[6], v[7]);
         *reinterpret_cast<uint4*>(dst) = raw;
       }
     }
@@ -656,7 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (sc.i_lo + it % nt) * kBM;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        float* dst = p.dq_acc + ((size_t)(b * a.h + hq) * p.lq_pad + q0 + 64 * h) * D + dd;
+        // accumulator layout [n h][lq_pad / 4][D][4]: four consecutive query rows per head-dim index
+        float* dst = p.dq_acc + (((size_t)(b * a.h + hq) * p.lq_pad + q0 + 64 * h) / 4 * D + dd) * 4;
         if (ok) ok = warp_wait_parity(&dq_full[h], it & 1, abort_flag, p.status);
         if (!ok) {
           if (more) named_bar_sync(kDqEmptyBar + h, kDqEmptyThreads);  // aborted: keep the phases matched
@@ -672,10 +670,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         if (more) named_bar_arrive(kDqEmptyBar + h, kDqEmptyThreads);
         if (live) {
-          // lanes of a warp hold 32 consecutive head-dim entries of one query row:
-          // each reduction instruction covers one contiguous 128-byte line
+          // a thread adds four query rows of its head-dim entry per instruction; the 32 lanes
+          // of a warp cover 32 consecutive entries, one contiguous 512-byte span
 #pragma unroll
-          for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)c * D, __uint_as_float(v[c]));
+          for (int u = 0; u < 16; ++u)
+            red_add_v4(dst + (size_t)u * D * 4, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                       __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
         }
       }
     }
@@ -750,11 +750,12 @@ cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUt
 }
 
 cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch) {
-  const int64_t qrows = (int64_t)p.a.n * p.a.h * p.a.lq;
-  if (qrows == 0) return cudaSuccess;
+  const int64_t groups = (int64_t)p.a.n * p.a.h * ((p.a.lq + 3) / 4);
+  if (groups == 0) return cudaSuccess;
   auto kern = (p.a.d == 128) ? bwd_convert_dq_kernel<128> : bwd_convert_dq_kernel<64>;
   unsigned grid = 0;
-  cudaError_t e = row_grid(kern, qrows, p.a.d, &grid);
+  // row_grid counts two rows per thread group and pass; the convert takes one group of four
+  cudaError_t e = row_grid(kern, 2 * groups, p.a.d, &grid);
   if (e != cudaSuccess) return e;
   kern<<<grid, kRowThreads, 0, s>>>(p);
   *nlaunch += 1;

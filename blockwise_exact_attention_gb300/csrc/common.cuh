@@ -86,7 +86,7 @@ struct BwdParams {
   int out_is_f32, dq_is_f32, dk_is_f32, dv_is_f32;
   Lse3 lse;
   int accumulate;
-  float* dq_acc;  // workspace: fp32 dQ partial sums, tile-major (see bwd_sm103.cu)
+  float* dq_acc;  // workspace: fp32 dQ partial sums, [n h][lq_pad / 4][d][4] (four query rows interleaved)
   float* d_row;   // workspace: [n, h, lq_pad] D = rowsum(dO * O)
   float* lse2;    // workspace: [n, h, lq_pad] lse * log2(e), +inf for rows without keys / padding
   int lq_pad;

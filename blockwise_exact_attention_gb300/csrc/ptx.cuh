@@ -401,6 +401,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Four fp32 additions into global memory (16-byte aligned), no result returned.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // Packed pairs of fp32 (the .f32x2 forms of sm_100 and later: one instruction
 // for two lanes of fma/add/mul, each rounded to nearest like its scalar form).
 __device__ __forceinline__ uint64_t f2(float a, float b) {
