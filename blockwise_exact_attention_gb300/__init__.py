@@ -28,6 +28,7 @@ from .ops import (  # noqa: F401
     launches_since_reset,
     ring_merge,
     selftest_wait_timeout,
+    selftest_inject_abort,
 )
 from .ring import chunk_schedule, ring_attention_bwd, ring_attention_fwd  # noqa: F401
 from .autograd import flash_attention, ring_attention  # noqa: F401,E402

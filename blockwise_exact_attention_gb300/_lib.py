@@ -40,6 +40,7 @@ EXPORTS = (
     "bea_status_string",
     "bea_version",
     "bea_selftest_wait_timeout",
+    "bea_selftest_inject_abort",
     "bea_last_launch_count",
     "bea_flash_mha_bwd_noalloc",
     "bea_flash_mha_bwd_prepare",
@@ -96,6 +97,8 @@ def load() -> ctypes.CDLL:
     lib.bea_version.restype = i
     lib.bea_selftest_wait_timeout.argtypes = [i, vp]
     lib.bea_selftest_wait_timeout.restype = i
+    lib.bea_selftest_inject_abort.argtypes = [i]
+    lib.bea_selftest_inject_abort.restype = i
     lib.bea_last_launch_count.argtypes = []
     lib.bea_last_launch_count.restype = i
     lib.bea_flash_mha_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, f, i, i, i, i, vp]

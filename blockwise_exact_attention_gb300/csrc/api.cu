@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -43,6 +44,10 @@ int status_ptr_for_current_device(uint32_t** out) {
   *out = g_status_ptr[dev];
   return BEA_OK;
 }
+
+// Pending abort injection (tile + 1, 0 = none), taken by the next main-kernel launch.
+std::atomic<int> g_inject_abort{0};
+int take_inject_abort() { return g_inject_abort.exchange(0); }
 
 int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -283,6 +288,7 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
   p.lse = lse3(lse);
   p.merge = 0;
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  p.inject_abort = take_inject_abort();
   CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
@@ -320,6 +326,7 @@ int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_
   p.merge = 1;
   p.fin = out_final ? seq4(out_final) : Seq4{nullptr, 0, 0, 0};
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  p.inject_abort = take_inject_abort();
   CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
@@ -385,6 +392,7 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
   p.accumulate = accumulate;
   set_workspace(&p, workspace, w);
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  p.inject_abort = take_inject_abort();
   CUtensorMap tq, tk, tv, tdo;
   std::memset(&tq, 0, sizeof(tq));
   std::memset(&tk, 0, sizeof(tk));
@@ -451,6 +459,7 @@ int bea_flash_mha_bwd_kv_block(const bea_tensor* dout, const bea_tensor* q, cons
   p.accumulate = accumulate;
   set_workspace(&p, workspace, w);
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
+  p.inject_abort = take_inject_abort();
   CUtensorMap tq, tk, tv, tdo;
   std::memset(&tq, 0, sizeof(tq));
   std::memset(&tk, 0, sizeof(tk));
@@ -527,6 +536,12 @@ int bea_get_device_status(void* stream) {
   if (cudaDeviceSynchronize() != cudaSuccess) return BEA_ERR_CUDA;
   if (word & bea::BEA_STATUS_TIMEOUT) return BEA_ERR_TIMEOUT;
   if (word & bea::BEA_STATUS_CONFIG) return BEA_ERR_UNSUPPORTED;
+  return BEA_OK;
+}
+
+int bea_selftest_inject_abort(int tile) {
+  if (tile < -1) return BEA_ERR_ARG;
+  g_inject_abort.store(tile + 1);
   return BEA_OK;
 }
 

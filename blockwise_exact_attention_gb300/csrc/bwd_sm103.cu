@@ -69,21 +69,21 @@ static_assert(2 * kRegsCompute + kRegsDrain + kRegsOther == 4 * kRegsLaunch, "re
 constexpr int kDrainWarp0 = 8;  // warps 8-11
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
-// Thread-to-MMA-warp hand-offs go over hardware named barriers (one phase per
-// tile and half; barrier 0 is __syncthreads):
-//   kReadyBar + h    "P_h^T / dS_h^T written": the 8 key warps and the MMA warp;
-//   kDqEmptyBar + h  "dQ_h^T read out of slot h": the 4 drain warps and the MMA
-//                    warp, for every tile but the last (no slot reuse after it).
-// A named barrier has no time limit, so the phases stay matched on every path.
-// Producers arrive without waiting on the normal path; they cannot reach the
-// next phase of the same barrier before the MMA warp has passed this one (that
-// needs an MMA it issues afterwards). After an abort every side keeps joining
-// the remaining phases without work, the producers with a waiting sync so that
-// none runs a phase ahead.
+// "P_h^T / dS_h^T written" goes from the 8 key warps to the MMA warp over
+// hardware named barrier kReadyBar + h (one phase per tile; barrier 0 is
+// __syncthreads). "dQ_h^T read out of slot h" goes from the drain to the MMA
+// warp over an mbarrier: the drain must start its reductions at once, and an
+// mbarrier arrival does not wait.
+// A named barrier has no time limit, so the phases stay matched on every path:
+// every side joins every phase of a barrier once, in tile/half order, with or
+// without work (after an abort), and every join waits for the phase to
+// complete (barrier.sync, never a bare arrive). No warp can then join phase
+// k+1 while phase k is open; a bare arrive followed by an aborting warp's next
+// join could land both in one phase and leave a later phase short. The key
+// warps' next step waits for an MMA the MMA warp issues only after this phase,
+// so the wait costs them nothing.
 constexpr uint32_t kReadyBar = 1;
 constexpr uint32_t kReadyThreads = 256 + 32;
-constexpr uint32_t kDqEmptyBar = 3;
-constexpr uint32_t kDqEmptyThreads = 128 + 32;
 
 template <int D>
 struct BwdCfg {
@@ -97,7 +97,7 @@ struct BwdCfg {
   static constexpr int kDSBytes = 128 * 128 * 2;
   static constexpr int kRowOff = kDSOff + kDSBytes;         // 2 stages of L2[128], D[128] fp32
   static constexpr int kBarOff = kRowOff + 2 * 1024;
-  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);    // S_h^T, dP_h^T
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, false, true);     // dV (TMEM A), dK
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qdo_empty = do_full + 2;
   uint64_t* sp_full = qdo_empty + 2;  // [2]: S_h^T and dP_h^T of half h are in TMEM slot h
   uint64_t* dq_full = sp_full + 2;    // [2]: dQ_h^T in TMEM slot h
-  uint64_t* dkv_full = dq_full + 2;
+  uint64_t* dq_empty = dq_full + 2;   // [2]: dQ_h^T read out of slot h (128 drain threads arrive)
+  uint64_t* dkv_full = dq_empty + 2;
   uint64_t* mma_done = dkv_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qdo_empty[s], 1);
       mbar_init(&sp_full[s], 1);
       mbar_init(&dq_full[s], 1);
+      mbar_init(&dq_empty[s], 128);
     }
     mbar_init(dkv_full, 1);
     mbar_init(mma_done, 1);
@@ -503,8 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_dp(1, 0);
         umma_commit_warp(&sp_full[1]);
       }
-      int n_ready = 0, n_dq_empty = 0;  // named-barrier phases joined, in (tile, half) order
+      int n_ready = 0;  // named-barrier phases joined, in (tile, half) order
       for (int it = 0; ok && it < sc.n_iter; ++it) {
+        if (p.inject_abort == it + 1 && blockIdx.x == 0) {
+          // test hook: behave exactly as if a wait of this warp had run out of time here
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_status(p.status, BEA_STATUS_TIMEOUT);
+          }
+          ok = false;
+          break;
+        }
         const int s = it & 1, s1 = s ^ 1;
         const uint32_t par1 = ((it + 1) >> 1) & 1;
         const bool more = it + 1 < sc.n_iter;
@@ -522,8 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_s(h, s1);
             // dQ_h^T of tile i occupies the dP_h^T columns until the drain has read it
-            named_bar_sync(kDqEmptyBar + h, kDqEmptyThreads);
-            ++n_dq_empty;
+            if (!(ok = warp_wait_parity(&dq_empty[h], it & 1, abort_flag, p.status))) break;
             if (h == 0 && !(ok = warp_wait_parity(&do_full[s1], par1, abort_flag, p.status))) break;
             tc_fence_after();
             issue_dp(h, s1);
@@ -533,8 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // After an abort, join the phases not reached, in the order the other side joins them.
       for (; n_ready < 2 * sc.n_iter; ++n_ready) named_bar_sync(kReadyBar + (n_ready & 1), kReadyThreads);
-      for (; n_dq_empty < 2 * (sc.n_iter - 1); ++n_dq_empty)
-        named_bar_sync(kDqEmptyBar + (n_dq_empty & 1), kDqEmptyThreads);
       if (ok && sc.n_iter > 0) umma_commit_warp(dkv_full);
       umma_commit_warp(mma_done);
       volatile int no_abort = 0;
@@ -582,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
-        named_bar_arrive(kReadyBar + h, kReadyThreads);
+        named_bar_sync(kReadyBar + h, kReadyThreads);
       }
     }
     // ---- dK / dV epilogue: key warpgroup 0 writes dV, warpgroup 1 writes dK ----
@@ -647,19 +655,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
     const bool live = dd < D;  // for d = 64 the upper 64 lanes hold padding rows
     bool ok = true;
-    for (int it = 0; it < sc.n_iter; ++it) {
+    for (int it = 0; ok && it < sc.n_iter; ++it) {
       const int hq = kvh * sc.g + it / nt;
-      const bool more = it + 1 < sc.n_iter;  // the MMA warp reuses the slot only for a next tile
       const int q0 = (sc.i_lo + it % nt) * kBM;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         // accumulator layout [n h][lq_pad / 4][D][4]: four consecutive query rows per head-dim index
         float* dst = p.dq_acc + (((size_t)(b * a.h + hq) * p.lq_pad + q0 + 64 * h) / 4 * D + dd) * 4;
         if (ok) ok = warp_wait_parity(&dq_full[h], it & 1, abort_flag, p.status);
-        if (!ok) {
-          if (more) named_bar_sync(kDqEmptyBar + h, kDqEmptyThreads);  // aborted: keep the phases matched
-          continue;
-        }
+        if (!ok) break;
         tc_fence_after();
         uint32_t v[64];
         const uint32_t dq_t = tmem + lane_base + 128u * h + T_DP;
@@ -668,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence<64>(v);
         tc_fence_before();
-        if (more) named_bar_arrive(kDqEmptyBar + h, kDqEmptyThreads);
+        mbar_arrive(&dq_empty[h]);  // the slot is free for the next tile's dP_h^T
         if (live) {
           // a thread adds four query rows of its head-dim entry per instruction; the 32 lanes
           // of a warp cover 32 consecutive entries, one contiguous 512-byte span

@@ -75,6 +75,7 @@ struct FwdParams {
   int merge;  // fold the block into (out, lse) instead of writing it
   Seq4 fin;   // merge only: bf16 copy of the merged rows, ptr may be null
   uint32_t* status;
+  int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at tile inject_abort - 1
 };
 // Tensor maps are built by the caller (api.cu) over q, k, v.
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -91,6 +92,7 @@ struct BwdParams {
   float* lse2;    // workspace: [n, h, lq_pad] lse * log2(e), +inf for rows without keys / padding
   int lq_pad;
   uint32_t* status;
+  int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at iteration inject_abort - 1
 };
 // Tensor maps over q, k, v, dout are built by the caller (api.cu).
 // launch_bwd_bf16 = prepare (D, lse*log2e, zeroed dQ accumulator) + main

@@ -57,10 +57,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when th
 // matched on every path:
 //  * the MMA warp joins once per tile of subtile t; after an abort it still
 //    joins, without work, for each tile it has not reached;
-//  * each softmax warp joins once per tile of its range. On the normal path it
-//    arrives without waiting: it cannot reach tile j+1 before S_t(j+1), which
-//    the MMA warp issues only after phase j. After an abort it joins with a
-//    waiting sync, so that it never runs a phase ahead of the MMA warp.
+//  * each softmax warp joins once per tile of its range, with or without work.
+//  * Every join waits for the phase to complete (barrier.sync, never a bare
+//    arrive), so no warp can join phase j+1 while phase j is still open: a
+//    bare arrive followed by an aborting warp's next join could land both in
+//    one phase and leave a later phase short of arrivals. The wait costs the
+//    softmax nothing, as its next step waits for S_t(j+1), which the MMA warp
+//    issues only after phase j.
 constexpr uint32_t kPReadyBar = 1;
 constexpr uint32_t kPReadyThreads = 128 + 32;
 
@@ -286,6 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int it = 0;
         for (int j = lo_all; ok && j < hi_all; ++j, ++it) {
+          if (p.inject_abort == it + 1 && blockIdx.x == 0) {
+            // test hook: behave exactly as if a wait of this warp had run out of time here
+            if (lane == 0) {
+              *abort_flag = 1;
+              report_status(p.status, BEA_STATUS_TIMEOUT);
+            }
+            ok = false;
+            break;
+          }
           const int s = it % C::kStages;
           const uint32_t par = (it / C::kStages) & 1;
           const int s1 = (it + 1) % C::kStages;
@@ -434,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      named_bar_arrive(kPReadyBar + t, kPReadyThreads);
+      named_bar_sync(kPReadyBar + t, kPReadyThreads);
     }
     // ---- epilogue ----
     const bool have_o = my_lo < my_hi;

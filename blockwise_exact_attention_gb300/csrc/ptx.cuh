@@ -377,15 +377,11 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // named (hardware) barriers
 // ---------------------------------------------------------------------------
 
-// Arrive on named barrier `id` without waiting; `nthreads` (a multiple of 32)
-// is the barrier's total participant count.
-__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
-  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Arrive on named barrier `id` and wait for `nthreads` arrivals. The warp is
-// reconverged first. A named barrier has no time limit: every use pairs it
-// with producers that arrive on every path, aborts included.
+// Join named barrier `id` and wait until `nthreads` threads (a multiple of 32)
+// have joined this phase. The warp is reconverged first. A named barrier has
+// no time limit: every use joins each phase exactly once on every path, aborts
+// included, and always waits (a bare arrive could let a warp join the next
+// phase while this one is still open).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   __syncwarp();
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

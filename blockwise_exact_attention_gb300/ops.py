@@ -203,3 +203,9 @@ def device_status() -> int:
 
 def selftest_wait_timeout(limit_us: int) -> None:
     _lib.check(_lib.load().bea_selftest_wait_timeout(int(limit_us), _stream()), "selftest_wait_timeout")
+
+
+def selftest_inject_abort(tile: int) -> None:
+    """Arm a one-shot abort of the next forward/backward main-kernel launch at
+    tile `tile` of its first CTA (-1 disarms); see bea_selftest_inject_abort."""
+    _lib.check(_lib.load().bea_selftest_inject_abort(int(tile)), "selftest_inject_abort")

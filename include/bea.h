@@ -280,6 +280,20 @@ int bea_version(void);
  */
 int bea_selftest_wait_timeout(int limit_us, void* stream);
 
+/*
+ * Failure-detection self test of the attention kernels. Arms a one-shot
+ * injection: the next bf16 forward or backward main-kernel launch of this
+ * process (bea_flash_mha_fwd, _fwd_merge, _bwd, _bwd_kv_block, _bwd_noalloc)
+ * behaves in its first CTA as if a wait of the MMA-issuing warp had run out of
+ * time at tile (forward) or iteration (backward) `tile`. That CTA raises its
+ * abort flag and records BEA_STATUS_TIMEOUT. Every other role of the CTA then
+ * leaves its loop on its next wait, in-flight copies land, TMEM is freed and
+ * the kernel returns normally. The outputs of that launch are undefined; the
+ * status word reads BEA_ERR_TIMEOUT afterwards. `tile` = -1 disarms.
+ * Returns BEA_ERR_ARG for tile < -1. Nothing traps or faults.
+ */
+int bea_selftest_inject_abort(int tile);
+
 /* Number of kernels the last successful call on this host thread launched. */
 int bea_last_launch_count(void);
 
