@@ -443,48 +443,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_h^T = K Q_h^T (M = keys, N = 64 queries, K = d; both K-major) into slot h. It
       // overwrites P_h^T of the previous tile, which that tile's dV product (issued
       // earlier) consumed.
+      // descriptors as 32-bit halves: each operand step below is one 32-bit add
+      const SDesc k_kmaj2 = sdesc_split(k_kmaj), k_mn2 = sdesc_split(k_mn), v_kmaj2 = sdesc_split(v_kmaj);
+      const SDesc ds_mn2 = sdesc_split(ds_mn), q_kmaj2 = sdesc_split(q_kmaj0), q_mn2 = sdesc_split(q_mn0);
+      const SDesc do_kmaj2 = sdesc_split(do_kmaj0), do_mn2 = sdesc_split(do_mn0);
       auto issue_s = [&](int h, int st) {
-        const uint64_t qd = sdesc_add(q_kmaj0, st * C::kTileBytes + h * 8192);
+        const SDesc qd = sdesc_at(q_kmaj2, st * C::kTileBytes + h * 8192);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss_warp(tmem + 128u * h, sdesc_add(k_kmaj, off), sdesc_add(qd, off), C::kIdescS, k > 0 ? 1u : 0u);
+          umma_ss_warp(tmem + 128u * h, sdesc_at(k_kmaj2, off), sdesc_at(qd, off), C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
       // dP_h^T = V dO_h^T into the second half of slot h (where dQ_h^T of the previous tile
       // was: the caller has waited for the drain)
       auto issue_dp = [&](int h, int st) {
-        const uint64_t dd = sdesc_add(do_kmaj0, st * C::kTileBytes + h * 8192);
+        const SDesc dd = sdesc_at(do_kmaj2, st * C::kTileBytes + h * 8192);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(v_kmaj, off), sdesc_add(dd, off), C::kIdescS,
+          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_at(v_kmaj2, off), sdesc_at(dd, off), C::kIdescS,
                        k > 0 ? 1u : 0u);
         }
       };
       // dQ_h^T = K^T dS_h^T (A = K read MN-major, B = dS_h^T from shared memory, MN-major)
       // into the second half of slot h.
       auto issue_dq = [&](int h) {
+        const SDesc dsh = sdesc_at(ds_mn2, h * 16384);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_add(k_mn, k * 2048), sdesc_add(ds_mn, h * 16384 + k * 2048),
-                       C::kIdescQ, k > 0 ? 1u : 0u);
+          umma_ss_warp(tmem + 128u * h + T_DP, sdesc_at(k_mn2, k * 2048), sdesc_at(dsh, k * 2048), C::kIdescQ,
+                       k > 0 ? 1u : 0u);
       };
       // dV += P_h^T dO_h (A = P_h^T from TMEM, B = dO MN-major); dK += dS_h^T Q_h (A = dS_h^T
       // from TMEM, B = Q MN-major). Query step k (16 queries) of the half was formed by key
       // warpgroup k / 2, whose P^T / dS^T columns are [128h + 32 (k / 2), +16) /
       // [128h + 32 (k / 2) + 16, +16).
       auto issue_dkv = [&](int h, int st, bool first) {
-        const uint64_t q_mn = sdesc_add(q_mn0, st * C::kTileBytes);
-        const uint64_t do_mn = sdesc_add(do_mn0, st * C::kTileBytes);
+        const SDesc q_mn = sdesc_at(q_mn2, st * C::kTileBytes + h * 8192);
+        const SDesc do_mn = sdesc_at(do_mn2, st * C::kTileBytes + h * 8192);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ts_warp(tmem + T_DV, tmem + 128u * h + 32 * (k / 2) + 8 * (k % 2), sdesc_add(do_mn, (4 * h + k) * 2048),
+          umma_ts_warp(tmem + T_DV, tmem + 128u * h + 32 * (k / 2) + 8 * (k % 2), sdesc_at(do_mn, k * 2048),
                        C::kIdescKV, (!first || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ts_warp(tmem + T_DK, tmem + 128u * h + 32 * (k / 2) + 16 + 8 * (k % 2),
-                       sdesc_add(q_mn, (4 * h + k) * 2048), C::kIdescKV, (!first || k > 0) ? 1u : 0u);
+          umma_ts_warp(tmem + T_DK, tmem + 128u * h + 32 * (k / 2) + 16 + 8 * (k % 2), sdesc_at(q_mn, k * 2048),
+                       C::kIdescKV, (!first || k > 0) ? 1u : 0u);
       };
       // Issue order: S_0 dP_0 S_1 dP_1 (tile 0), then per tile i
       //   [P_0/dS_0 ready] dQ_0^T, dV, dK (i), S_0 dP_0 (tile i+1)

@@ -297,6 +297,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// A descriptor split into its 32-bit halves. The start address lives in the
+// low half and never carries out of its 14 bits (shared memory is < 256 KB),
+// so an operand further on is one 32-bit add on `lo`.
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_split(uint64_t d) { return {(uint32_t)d, (uint32_t)(d >> 32)}; }
+__device__ __forceinline__ SDesc sdesc_at(SDesc d, uint32_t bytes) { return {d.lo + (bytes >> 4), d.hi}; }
+
 // Descriptor of the same operand `bytes` further on: the start address sits
 // in the low 14 bits in 16-byte units and never carries out of them (shared
 // memory is < 256 KB), so advancing is one 64-bit add.
@@ -345,6 +354,30 @@ __device__ __forceinline__ void umma_ss_warp(uint32_t d_tmem, uint64_t adesc, ui
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// As umma_ss_warp, with both descriptors passed as 32-bit halves.
+__device__ __forceinline__ void umma_ss_warp(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %2};\n\t"
+      "mov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
+// As umma_ts_warp, with the B descriptor passed as 32-bit halves.
+__device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
