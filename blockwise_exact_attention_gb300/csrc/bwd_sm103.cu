@@ -21,9 +21,9 @@
 //        warp 13     MMA issuer (the whole warp, one elected lane issues):
 //                    per half h, S_h^T = K Q_h^T and dP_h^T = V dO_h^T into
 //                    TMEM slot h; then, per half as soon as its P^T / dS^T
-//                    are ready, dV += P_h^T dO_h and dK += dS_h^T Q_h (P^T,
-//                    dS^T from TMEM) and dQ_h^T = K^T dS_h^T (dS^T from
-//                    shared memory). Each half's products for this tile are
+//                    are ready, dQ_h^T = K^T dS_h^T (dS^T from shared
+//                    memory), dV += P_h^T dO_h and dK += dS_h^T Q_h (P^T,
+//                    dS^T from TMEM). Each half's products for this tile are
 //                    followed at once by that half's S^T / dP^T for the
 //                    next tile, so the key warps' work on one half hides
 //                    behind the tensor work of the other,
@@ -32,9 +32,9 @@
 //                    half from S^T, dP^T, L2, D; finally warpgroup 0 writes
 //                    dV and warpgroup 1 dK,
 //        warps 8-11  one thread per head-dim index: read dQ_h^T out of TMEM
-//                    and add it into the fp32 accumulator; the 32 lanes of a
-//                    warp cover 32 consecutive entries of a query row, so each
-//                    reduction instruction is one contiguous 128-byte line.
+//                    and add it into the fp32 accumulator, four query rows per
+//                    16-byte reduction; the 32 lanes of a warp cover 32
+//                    consecutive entries, one contiguous 512-byte span.
 //      Two TMEM slots let the tensor core compute one half while the key
 //      warps work on the other, and the drain of one half's dQ^T overlaps
 //      the other half's products. dK and dV accumulate in TMEM across the
