@@ -9,7 +9,9 @@
 // before the P V product.
 //
 // One CTA owns 256 query rows (two 128-row subtiles) of one (batch, head):
-//   warp 8      TMA producer: Q once, then K_j / V_j into an NS-stage ring;
+//   warp 8      TMA producer: Q once, then K_j into an NS-stage ring;
+//   warp 10     TMA producer of V_j, on its own ring (V_j is released after
+//               P V, K_j after the S of tile j);
 //   warp 9      MMA issuer (the whole warp runs the loop, one elected lane
 //               issues): S_t = Q_t K_j^T into TMEM (both operands in
 //               shared memory), O_t += P_t V_j with P_t read from TMEM;
