@@ -156,12 +156,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // Plain (non-tensor) bulk copy global -> shared, completion as transaction
 // bytes on `bar`. Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -174,23 +168,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Bulk (non-tensor) reduce-add of fp32 from shared to global memory.
-// Both addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -313,33 +290,12 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
   return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], operands as described. One thread issues.
-// No "memory" clobber: the MMA reads shared memory asynchronously, ordered by
-// the mbarrier waits (which do clobber memory) and by the program order of
-// volatile asm; a clobber here would only force needless reloads between
-// consecutive MMAs of the issuing thread.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]. A is M rows (lanes) x K packed bf16 pairs
-// (element 2c in the low half of column c). One thread issues.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-// Warp forms of the three issue calls above: all 32 lanes of the warp call
-// them together (converged) and elect.sync picks the one lane that issues.
+// MMA issue and commit, called by all 32 lanes of a warp together (converged);
+// elect.sync picks the one lane that issues. D[tmem] (+)= A * B with A from
+// shared memory (SS form) or TMEM (TS form: M rows = lanes, K packed bf16
+// pairs, element 2c in the low half of column c), B from shared memory. No
+// "memory" clobber: the MMA reads shared memory asynchronously, ordered by the
+// mbarrier waits (which clobber memory) and the program order of volatile asm.
 // A warp that runs its whole MMA loop this way keeps the descriptor
 // arithmetic warp-uniform; an issuing thread alone in its warp, by contrast,
 // loses issue slots to busy warps on the same scheduler and feeds the tensor
@@ -396,14 +352,6 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
-}
-
-// Arrive once on `bar` when all previously issued tcgen05 MMAs of this
-// thread have completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
 }
 
 // ---------------------------------------------------------------------------
