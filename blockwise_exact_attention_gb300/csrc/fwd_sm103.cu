@@ -434,8 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(s_tmem + 0, pk);
       tmem_st32(s_tmem + 32, pk + 32);
       if (rescale) {
-        // PV_t(j-1) has completed: s_full for tile j was committed after it.
-#pragma unroll
+        // PV_t(j-1) has completed: s_full for tile j was committed after it. Rare (the row max
+        // grew by more than 2^8): a rolled loop, which keeps the register demand of the tile
+        // loop down (unrolled, it makes the compiler spill around it on every tile).
+#pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t orow[32];
           tmem_ld32(o_tmem + c0, orow);
