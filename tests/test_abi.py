@@ -202,3 +202,6 @@ def test_merge_rejects_bad_arguments(lib):
 def test_selftest_argument_range(lib):
     assert lib.bea_selftest_wait_timeout(0, None) == ARG
     assert lib.bea_selftest_wait_timeout(2000001, None) == ARG
+    assert lib.bea_selftest_inject_abort(-2) == ARG
+    assert lib.bea_selftest_inject_abort(3) == 0     # armed (one-shot) ...
+    assert lib.bea_selftest_inject_abort(-1) == 0    # ... and disarmed again before any launch
