@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it & 1, s1 = s ^ 1;
         const uint32_t par1 = ((it + 1) >> 1) & 1;
         const bool more = it + 1 < sc.n_iter;
-#pragma unroll 1
+#pragma unroll
         for (int h = 0; h < 2; ++h) {
           named_bar_sync(kReadyBar + h, kReadyThreads);  // P_h^T / dS_h^T of tile it are written
           ++n_ready;
