@@ -247,6 +247,15 @@ def run_only(which, fwd, bwd, dev, workloads, bea):
         fwd()
         for _ in range(4):
             bwd()
+    elif which == "bwd_d64":
+        # the d=64 full-attention workload [1,32768,32,64] of the measurement plan
+        wo = workloads.WORKLOADS["full_32k_d64"]
+        qo = torch.randn((wo.n, wo.l, wo.h, wo.d), device=dev).to(torch.bfloat16)
+        ko = torch.randn((wo.n, wo.l, wo.h_kv, wo.d), device=dev).to(torch.bfloat16)
+        vo, doo = torch.randn_like(ko), torch.randn_like(qo)
+        oo, lo_ = bea.flash_mha_fwd(qo, ko, vo, wo.softmax_scale, wo.is_causal, wo.window)
+        for _ in range(4):
+            bea.flash_mha_bwd(doo, qo, ko, vo, oo, lo_, wo.softmax_scale, wo.is_causal, wo.window)
     else:
         wr = workloads.WORKLOADS["ring_causal_16k"]
         acc = torch.randn((1, wr.l, wr.h, wr.d), device=dev)
@@ -267,8 +276,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fwd", "bwd", "merge"],
-                    help="run just this kernel a few times on the bench workload (for profiler captures)")
+    ap.add_argument("--only", choices=["fwd", "bwd", "merge", "bwd_d64"],
+                    help="run just this kernel a few times on the bench workload, or bwd_d64 on the d=64 "
+                         "full-attention workload (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -340,10 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   // ---- work: key blocks in ascending order (under a causal mask the first see the most queries) ----
+  // Without a mask band every CTA has the same work. With one query head per K/V head the
+  // CTAs are then taken head by head, so that the ones running together share one head's
+  // Q/dO tiles and dQ accumulator rows in L2 (measured: 32k d=64 full attention -12%, 8k d=128
+  // -6%). Under a causal or window band the key blocks go in ascending order (longest first),
+  // and so do grouped heads (their 4x longer CTAs measured 3% slower head by head).
   const int nkv = a.n * a.hkv;
-  const int kb = blockIdx.x / nkv;
-  const int b = (blockIdx.x % nkv) / a.hkv;
-  const int kvh = (blockIdx.x % nkv) % a.hkv;
+  const int nkb = (a.lk + kBN - 1) / kBN;
+  const bool head_major = a.wl >= kUnbounded && a.wr >= kUnbounded && a.h == a.hkv;
+  const int kb = head_major ? (int)(blockIdx.x % nkb) : (int)(blockIdx.x / nkv);
+  const int bkv = head_major ? (int)(blockIdx.x / nkb) : (int)(blockIdx.x % nkv);
+  const int b = bkv / a.hkv;
+  const int kvh = bkv % a.hkv;
   BwdSched sc;
   sc.k0 = kb * kBN;
   sc.g = a.h / a.hkv;

@@ -138,8 +138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work decomposition: longest (latest) query blocks first ----
   const int nqb = (a.lq + kSub * kBlockM - 1) / (kSub * kBlockM);
   const int bh_count = a.n * a.h;
-  const int qb = nqb - 1 - (int)(blockIdx.x / bh_count);
-  const int bh = blockIdx.x % bh_count;
+  // Without a mask band every CTA has the same work. With one query head per K/V head the
+  // CTAs are then taken head by head, so that the ones running together stream one head's K/V
+  // tiles from L2 (measured: 32k d=64 full attention -2%). Under a causal or window band the
+  // latest (longest) query blocks go first.
+  const bool head_major = a.wl >= kUnbounded && a.wr >= kUnbounded && a.h == a.hkv;
+  const int qb = head_major ? nqb - 1 - (int)(blockIdx.x % nqb) : nqb - 1 - (int)(blockIdx.x / bh_count);
+  const int bh = head_major ? (int)(blockIdx.x / nqb) : (int)(blockIdx.x % bh_count);
   const int b = bh / a.h, hq = bh % a.h, kvh = hq / (a.h / a.hkv);
   Sched sc;
   sc.q0 = qb * kSub * kBlockM;
