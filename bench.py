@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20
 # `bench.py --only {fwd,bwd,merge}`. A kernel changed since its capture gets
 # None here until it is captured again.
 NCU_TRAFFIC_BYTES = {
-    "bwd_bf16_kernel<128>": 598.6e6 + 267.8e6,   # causal GQA 8k, one launch
-    "fwd_bf16_kernel<128>": 100.8e6 + 31.7e6,    # causal GQA 8k, one launch
+    "bwd_bf16_kernel<128>": 611.1e6 + 271.7e6,   # causal GQA 8k, one launch
+    "fwd_bf16_kernel<128>": 100.9e6 + 31.9e6,    # causal GQA 8k, one launch
     "ring_merge_kernel": 204.1e6 + 76.0e6,       # [1,16384,16,128]; second of back-to-back launches
 }
 
