@@ -52,7 +52,9 @@
  *   per-device status word, which bea_get_device_status() reads.
  *
  * Thread safety: calls may come from several host threads; the library's
- * only host state is a per-device cache filled on first use.
+ * host state is a per-device cache filled on first use and the one-shot test
+ * hook armed by bea_selftest_inject_abort (process-wide: the next launch from
+ * any thread takes it).
  */
 #ifndef BEA_H_
 #define BEA_H_
