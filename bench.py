@@ -37,14 +37,37 @@ WORKLOAD = "causal_gqa_8k_rope"
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# each kernel on the workloads below, from one `ncu --set full` capture of
-# `bench.py --only {fwd,bwd,merge}`. A kernel changed since its capture gets
-# None here until it is captured again.
-NCU_TRAFFIC_BYTES = {
-    "bwd_bf16_kernel<128>": 611.1e6 + 271.7e6,   # causal GQA 8k, one launch
-    "fwd_bf16_kernel<128>": 100.9e6 + 31.9e6,    # causal GQA 8k, one launch
-    "ring_merge_kernel": 204.1e6 + 76.0e6,       # [1,16384,16,128]; second of back-to-back launches
+# each kernel on the workloads below, from one ncu capture of
+# `bench.py --only {fwd,bwd,merge}` (profiles/), each with the hash of the
+# kernel sources it was taken on. When the current sources hash differently the
+# figure no longer describes the kernel, and the JSON line reports null.
+NCU_TRAFFIC = {
+    # kernel: (bytes per launch, source hash at capture)
+    "bwd_bf16_kernel<128>": (611.1e6 + 271.7e6, None),   # causal GQA 8k, one launch
+    "fwd_bf16_kernel<128>": (100.9e6 + 31.9e6, None),    # causal GQA 8k, one launch
+    "ring_merge_kernel": (204.1e6 + 76.0e6, None),       # [1,16384,16,128]
 }
+KERNEL_SOURCES = {
+    "bwd_bf16_kernel<128>": ("bwd_sm103.cu", "ptx.cuh", "common.cuh"),
+    "fwd_bf16_kernel<128>": ("fwd_sm103.cu", "ptx.cuh", "common.cuh"),
+    "ring_merge_kernel": ("merge.cu", "common.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 (first 12 hex digits) of the source files a kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "blockwise_exact_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str):
+    """The captured DRAM bytes per launch, or None when the sources changed since."""
+    nbytes, at = NCU_TRAFFIC[kernel]
+    return nbytes if at is not None and at == kernel_source_hash(kernel) else None
 
 
 def bench_config(world: int) -> dict:
@@ -256,6 +279,19 @@ def run_only(which, fwd, bwd, dev, workloads, bea):
         oo, lo_ = bea.flash_mha_fwd(qo, ko, vo, wo.softmax_scale, wo.is_causal, wo.window)
         for _ in range(4):
             bea.flash_mha_bwd(doo, qo, ko, vo, oo, lo_, wo.softmax_scale, wo.is_causal, wo.window)
+    elif which in ("ring", "ring_unfused", "ring_bwd"):
+        # the 16k causal ring replay (8 chunks): two forward replays, or two backward replays
+        wr = workloads.WORKLOADS["ring_causal_16k"]
+        qr = torch.randn((1, wr.l, wr.h, wr.d), device=dev).to(torch.bfloat16)
+        kr, vr, dor = torch.randn_like(qr), torch.randn_like(qr), torch.randn_like(qr)
+        if which == "ring_bwd":
+            o_r, l_r = bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True)
+            for _ in range(2):
+                bea.ring_attention_bwd(dor, qr, kr, vr, o_r, l_r, wr.ring_chunks, wr.softmax_scale, True)
+        else:
+            kw = {} if which == "ring" else {"block_dtype": torch.bfloat16, "fused": False}
+            for _ in range(2):
+                bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True, **kw)
     else:
         wr = workloads.WORKLOADS["ring_causal_16k"]
         acc = torch.randn((1, wr.l, wr.h, wr.d), device=dev)
@@ -276,9 +312,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fwd", "bwd", "merge", "bwd_d64"],
-                    help="run just this kernel a few times on the bench workload, or bwd_d64 on the d=64 "
-                         "full-attention workload (for profiler captures)")
+    ap.add_argument("--only", choices=["fwd", "bwd", "merge", "bwd_d64", "ring", "ring_unfused", "ring_bwd"],
+                    help="run just this kernel a few times on the bench workload, bwd_d64 on the d=64 "
+                         "full-attention workload, or two ring replays of the 16k causal workload "
+                         "(for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -394,43 +431,69 @@ def main():
     main_tf = f_bwd / (ms_main * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ----
+    # Every step uploads its q, k, v, dout from pinned host memory and reads out, lse,
+    # dq, dk, dv back, inside the timed region. Device buffers are double-buffered, so
+    # step s+1's uploads (copy-in stream) run while step s computes and step s-1's
+    # results come down (copy-out stream): the copies overlap compute instead of
+    # adding to it. ms_per_step = the time of K back-to-back steps / K.
     hq_, hk_, hv_, hdo_ = (t.cpu().pin_memory() for t in (q, k, v, do))
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h_dq, h_dk, h_dv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
     h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hdo_))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_dq, h_dk, h_dv))
+    bufs = [dict(q=q, k=k, v=v, do=do, out=out, lse=lse, dq=dq, dk=dk, dv=dv, ws=ws)]
+    bufs.append({key: torch.empty_like(t) for key, t in bufs[0].items()})
+    up_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev)
 
-    copy_stream = torch.cuda.Stream(device=dev)
+    def e2e_run(nsteps):
+        """nsteps end-to-end steps, pipelined over the two buffer sets; returns ms per step."""
+        free = [stream.record_event(), stream.record_event()]   # compute done with buffer set b
+        drained = [stream.record_event(), stream.record_event()]  # results of buffer set b read back
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        up_stream.wait_stream(stream)
+        down_stream.wait_stream(stream)
+        for st in range(nsteps):
+            bset = bufs[st % 2]
+            with torch.cuda.stream(up_stream):
+                up_stream.wait_event(free[st % 2])
+                bset["q"].copy_(hq_, non_blocking=True)
+                bset["k"].copy_(hk_, non_blocking=True)
+                bset["v"].copy_(hv_, non_blocking=True)
+                bset["do"].copy_(hdo_, non_blocking=True)
+                uploaded = up_stream.record_event()
+            stream.wait_event(uploaded)
+            stream.wait_event(drained[st % 2])   # the previous results in this set have come down
+            bea.flash_mha_fwd(bset["q"], bset["k"], bset["v"], s, True, out=bset["out"], lse=bset["lse"])
+            fwd_done = stream.record_event()
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(fwd_done)
+                h_out.copy_(bset["out"], non_blocking=True)
+                h_lse.copy_(bset["lse"], non_blocking=True)
+            bea.flash_mha_bwd(bset["do"], bset["q"], bset["k"], bset["v"], bset["out"], bset["lse"], s, True,
+                              dq=bset["dq"], dk=bset["dk"], dv=bset["dv"], workspace=bset["ws"])
+            free[st % 2] = stream.record_event()
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(free[st % 2])
+                h_dq.copy_(bset["dq"], non_blocking=True)
+                h_dk.copy_(bset["dk"], non_blocking=True)
+                h_dv.copy_(bset["dv"], non_blocking=True)
+                drained[st % 2] = down_stream.record_event()
+        stream.wait_stream(up_stream)
+        stream.wait_stream(down_stream)
+        t1.record(stream)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / nsteps
 
-    def e2e_step():
-        # q, k, v go up on the compute stream; dout goes up on a second stream while the
-        # forward runs, and out/lse come down there while the backward runs. The step
-        # ends on the compute stream once every copy has landed.
-        copy_stream.wait_stream(stream)          # the previous step is done with dout and out
-        q.copy_(hq_, non_blocking=True)
-        k.copy_(hk_, non_blocking=True)
-        v.copy_(hv_, non_blocking=True)
-        with torch.cuda.stream(copy_stream):
-            do.copy_(hdo_, non_blocking=True)
-            do_ready = copy_stream.record_event()
-        fwd()
-        fwd_done = stream.record_event()
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(fwd_done)
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
-            outs_down = copy_stream.record_event()
-        stream.wait_event(do_ready)
-        bwd()
-        h_dq.copy_(dq, non_blocking=True)
-        h_dk.copy_(dk, non_blocking=True)
-        h_dv.copy_(dv, non_blocking=True)
-        stream.wait_event(outs_down)
-
-    e2e_ms = statistics.mean(timed(e2e_step, max(3, args.steps // 4), 2))
+    e2e_run(3)
+    e2e_ms = e2e_run(max(6, args.steps))
     e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
     e2e_val = job_tflops(world, f_fwd + f_bwd, e2e_ms)
+    del bufs[1]
 
     # ---- ring_merge standalone, [1, 16384, 16, 128], L2 flushed ----
     wr = workloads.WORKLOADS["ring_causal_16k"]
@@ -452,9 +515,21 @@ def main():
     # the unfused replay: each block written out in bf16, then ring_merge
     ring_unfused_ms = statistics.median(timed(lambda: bea.ring_attention_fwd(
         qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True, block_dtype=torch.bfloat16, fused=False), 5, 2))
-    rf, _ = attention_flops(1, wr.h, wr.l, wr.l, wr.d, True)
+    rf, rb = attention_flops(1, wr.h, wr.l, wr.l, wr.d, True)
     single_ms = statistics.median(timed(lambda: bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True), 5, 2))
-    del qr, kr, vr, acc, lacc, blk, lblk
+    # the ring backward: every live chunk pair once, from the single call's out/lse
+    dor = torch.randn_like(qr)
+    o_r, l_r = bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True)
+    bea.launches_since_reset(reset=True)
+    bea.ring_attention_bwd(dor, qr, kr, vr, o_r, l_r, wr.ring_chunks, wr.softmax_scale, True)
+    ring_bwd_launches = bea.launches_since_reset(reset=True)
+    ring_bwd_ms = statistics.median(timed(lambda: bea.ring_attention_bwd(dor, qr, kr, vr, o_r, l_r, wr.ring_chunks,
+                                                                         wr.softmax_scale, True), 5, 2))
+    wsr = torch.empty(bea.bwd_workspace_bytes(qr), dtype=torch.uint8, device=dev)
+    gr = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (qr, kr, vr)]
+    single_bwd_ms = statistics.median(timed(lambda: bea.flash_mha_bwd(
+        dor, qr, kr, vr, o_r, l_r, wr.softmax_scale, True, dq=gr[0], dk=gr[1], dv=gr[2], workspace=wsr), 5, 2))
+    del qr, kr, vr, acc, lacc, blk, lblk, dor, o_r, l_r, wsr, gr
 
     # ---- the other workloads of the measurement plan: forward and backward alone ----
     others = {}
@@ -520,22 +595,33 @@ def main():
         # events around its launch; algorithmic work = the backward's 2.5 x forward FLOPs
         "roofline": {"bound": "tensor", "kernel": "bwd_bf16_kernel<128>", "ms": ms_main,
                      "achieved": main_tf, "peak": pk_burst, "unit": "TFLOP/s", "frac": main_tf / pk_burst,
-                     "traffic": NCU_TRAFFIC_BYTES["bwd_bf16_kernel<128>"],
+                     "traffic": ncu_traffic("bwd_bf16_kernel<128>"),
+                     "source_hash": kernel_source_hash("bwd_bf16_kernel<128>"),
                      "peak_kind": f"{pk_kind} bf16 burst (a ~2 ms step, L2 flushed before it)"},
         "roofline_fwd": {"bound": "tensor", "kernel": "fwd_bf16_kernel<128>", "ms": ms_fwd, "achieved": fwd_tf,
                          "peak": pk_burst, "unit": "TFLOP/s", "frac": fwd_tf / pk_burst,
-                         "traffic": NCU_TRAFFIC_BYTES["fwd_bf16_kernel<128>"]},
+                         "traffic": ncu_traffic("fwd_bf16_kernel<128>"),
+                         "source_hash": kernel_source_hash("fwd_bf16_kernel<128>")},
         "merge": {"kernel": "ring_merge [1,16384,16,128] f32 acc + bf16 blk", "ms": merge_ms,
                   "bytes": merge_bytes, "gbs": merge_gbs, "peak_gbs": pk_hbm, "frac": merge_gbs / pk_hbm,
-                  "bound": "hbm", "traffic": NCU_TRAFFIC_BYTES["ring_merge_kernel"]},
+                  "bound": "hbm", "traffic": ncu_traffic("ring_merge_kernel"),
+                  "source_hash": kernel_source_hash("ring_merge_kernel")},
         "ring": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks: the 36 chunk pairs in ring order, one "
                              "batched call per ring step, 28 pairs as fused ring steps (merge in the forward "
                              "epilogue); 15 launches", "ms": ring_ms,
                  "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms,
                  "unfused_ms": ring_unfused_ms, "unfused": "forward + ring_merge per ring step (bf16 blocks): 15 launches"},
+        "ring_bwd": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks: the backward of every live chunk pair "
+                                 "(36) once, fp32 dq/dk/dv accumulated over the pairs, from the final out/lse",
+                     "ms": ring_bwd_ms, "tflops": rb / (ring_bwd_ms * 1e-3) / 1e12, "launches": ring_bwd_launches,
+                     "single_call_ms": single_bwd_ms, "single_call_tflops": rb / (single_bwd_ms * 1e-3) / 1e12},
         "other_workloads": others,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "how": "public API (flash_mha_fwd, flash_mha_bwd) on inputs uploaded from pinned host memory "
+                       "every step, results read back every step; two device buffer sets, uploads and "
+                       "read-backs on their own streams overlapping the neighbouring steps' compute; "
+                       "time of back-to-back steps / steps"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "device_status": status,

@@ -14,6 +14,7 @@
 
 #include "../../include/bea.h"
 #include "common.cuh"
+#include "launch_cache.cuh"
 #include "status.cuh"
 
 namespace {
@@ -27,22 +28,21 @@ thread_local int g_last_launches = 0;
 // Status word of each device the library runs on: kernels OR flags into it.
 __device__ uint32_t g_status_word;
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-uint32_t* g_status_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bea::PerContext<uint32_t*> g_status_ptr;
 
 int status_ptr_for_current_device(uint32_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BEA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_status_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || p == nullptr) return BEA_ERR_CUDA;
-    g_status_ptr[dev] = static_cast<uint32_t*>(p);
-  }
-  *out = g_status_ptr[dev];
-  return BEA_OK;
+  const cudaError_t e = g_status_ptr.get(
+      [](uint32_t** v) {
+        void* p = nullptr;
+        cudaError_t r = cudaGetSymbolAddress(&p, g_status_word);
+        if (r == cudaSuccess && p == nullptr) r = cudaErrorInvalidSymbol;
+        *v = static_cast<uint32_t*>(p);
+        return r;
+      },
+      out);
+  return e == cudaSuccess ? BEA_OK : BEA_ERR_CUDA;
 }
 
 // Pending abort injection (tile + 1, 0 = none), taken by the next main-kernel launch.
@@ -64,13 +64,35 @@ int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return BEA_OK;
 }
 
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_fn_once;
+PFN_ctxGetCurrent g_ctx_get_current = nullptr;
+PFN_ctxGetId g_ctx_get_id = nullptr;
+
+void load_ctx_fns() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      fn != nullptr && q == cudaDriverEntryPointSuccess)
+    g_ctx_get_current = reinterpret_cast<PFN_ctxGetCurrent>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      fn != nullptr && q == cudaDriverEntryPointSuccess)
+    g_ctx_get_id = reinterpret_cast<PFN_ctxGetId>(fn);
+}
+
 int64_t esize(int32_t dtype) { return dtype == BEA_BF16 ? 2 : 4; }
 
 bool valid_dtype(int32_t dt) { return dt == BEA_BF16 || dt == BEA_F32; }
 
+// Element count, saturating (shapes are validated non-negative first).
 int64_t numel(const bea_tensor* t) {
   int64_t n = 1;
-  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  for (int i = 0; i < t->ndim; ++i) {
+    if (t->shape[i] == 0) return 0;
+    if (__builtin_mul_overflow(n, t->shape[i], &n)) n = INT64_MAX;
+  }
   return n;
 }
 
@@ -200,14 +222,26 @@ int finish(cudaError_t e, int launches) {
 struct BwdWorkspace {
   size_t dq_off, d_off, l_off, total;
 };
+// Byte sizes saturate at SIZE_MAX instead of wrapping: a size no buffer can
+// have, which check_workspace then rejects.
+size_t mul_sat(size_t a, size_t b) {
+  size_t r;
+  return __builtin_mul_overflow(a, b, &r) ? SIZE_MAX : r;
+}
+size_t add_sat(size_t a, size_t b) {
+  size_t r;
+  return __builtin_add_overflow(a, b, &r) ? SIZE_MAX : r;
+}
+
 BwdWorkspace bwd_workspace_layout(int64_t n, int64_t lq, int64_t h, int64_t d) {
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const int64_t lq_pad = (lq + 127) / 128 * 128;
+  auto up = [](size_t x) { return x > SIZE_MAX - 255 ? SIZE_MAX : (x + 255) / 256 * 256; };
+  const size_t lq_pad = mul_sat((size_t)(lq / 128 + (lq % 128 != 0)), 128);
+  const size_t rows = mul_sat(mul_sat((size_t)n, (size_t)h), lq_pad);
   BwdWorkspace w;
   w.dq_off = 0;
-  w.d_off = up((size_t)(n * h * lq_pad * d) * 4);
-  w.l_off = w.d_off + up((size_t)(n * h * lq_pad) * 4);
-  w.total = w.l_off + up((size_t)(n * h * lq_pad) * 4);
+  w.d_off = up(mul_sat(mul_sat(rows, (size_t)d), 4));
+  w.l_off = add_sat(w.d_off, up(mul_sat(rows, 4)));
+  w.total = add_sat(w.l_off, up(mul_sat(rows, 4)));
   return w;
 }
 
@@ -226,6 +260,32 @@ void set_workspace(bea::BwdParams* p, void* workspace, const BwdWorkspace& w) {
   p->lq_pad = (p->a.lq + 127) / 128 * 128;
 }
 
+// Every check of bea_flash_mha_bwd except the workspace's.
+int check_bwd_args(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k, const bea_tensor* v,
+                   const bea_tensor* out, const bea_tensor* lse, const bea_tensor* dq, const bea_tensor* dk,
+                   const bea_tensor* dv, float softmax_scale, int is_causal, int window_left, int window_right,
+                   int accumulate, AttnDims* a) {
+  int rc;
+  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, nullptr, a))) return rc;
+  if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(out, 4)) || (rc = check_tensor(dq, 4)) ||
+      (rc = check_tensor(dk, 4)) || (rc = check_tensor(dv, 4)))
+    return rc;
+  if (!same_shape(dout, q) || !same_shape(out, q) || !same_shape(dq, q) || !same_shape(dk, k) ||
+      !same_shape(dv, k))
+    return BEA_ERR_SHAPE;
+  if ((rc = check_lse(lse, *a))) return rc;
+  if (accumulate != 0 && accumulate != 1) return BEA_ERR_ARG;
+  if (dout->dtype != q->dtype) return BEA_ERR_DTYPE;
+  if (out->dtype != q->dtype && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  const bool f32 = q->dtype == BEA_F32;
+  for (const bea_tensor* g : {dq, dk, dv}) {
+    if (accumulate && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
+    if (f32 && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  }
+  if (f32 && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
+  return BEA_OK;
+}
+
 // Dims of a stage that sees only [n, lq, h, d] query-side tensors (bf16 path).
 int query_side_dims(const bea_tensor* t, AttnDims* a) {
   const int64_t d = t->shape[3];
@@ -241,6 +301,43 @@ int query_side_dims(const bea_tensor* t, AttnDims* a) {
 }
 
 }  // namespace
+
+namespace bea {
+
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_fn_once, load_ctx_fns);
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int check_bwd_call(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k, const bea_tensor* v,
+                   const bea_tensor* out, const bea_tensor* lse, const bea_tensor* dq, const bea_tensor* dk,
+                   const bea_tensor* dv, float softmax_scale, int is_causal, int window_left, int window_right,
+                   int accumulate, size_t* workspace_bytes) {
+  AttnDims a;
+  const int rc = check_bwd_args(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, is_causal, window_left,
+                                window_right, accumulate, &a);
+  if (rc == BEA_OK) *workspace_bytes = bwd_workspace_layout(a.n, a.lq, a.h, a.d).total;
+  return rc;
+}
+
+cudaError_t device_sm_count(int* sms) {
+  static PerContext<int> cache;
+  return cache.get(
+      [](int* v) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+      },
+      sms);
+}
+
+}  // namespace bea
 
 extern "C" {
 
@@ -348,23 +445,10 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
                       int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
   AttnDims a;
   int rc;
-  if ((rc = check_qkv(q, k, v, softmax_scale, is_causal, window_left, window_right, nullptr, &a))) return rc;
-  if ((rc = check_tensor(dout, 4)) || (rc = check_tensor(out, 4)) || (rc = check_tensor(dq, 4)) ||
-      (rc = check_tensor(dk, 4)) || (rc = check_tensor(dv, 4)))
+  if ((rc = check_bwd_args(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, is_causal, window_left, window_right,
+                           accumulate, &a)))
     return rc;
-  if (!same_shape(dout, q) || !same_shape(out, q) || !same_shape(dq, q) || !same_shape(dk, k) ||
-      !same_shape(dv, k))
-    return BEA_ERR_SHAPE;
-  if ((rc = check_lse(lse, a))) return rc;
-  if (accumulate != 0 && accumulate != 1) return BEA_ERR_ARG;
-  if (dout->dtype != q->dtype) return BEA_ERR_DTYPE;
-  if (out->dtype != q->dtype && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
   const bool f32 = q->dtype == BEA_F32;
-  for (const bea_tensor* g : {dq, dk, dv}) {
-    if (accumulate && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
-    if (f32 && g->dtype != BEA_F32) return BEA_ERR_DTYPE;
-  }
-  if (f32 && out->dtype != BEA_F32) return BEA_ERR_DTYPE;
   const BwdWorkspace w = bwd_workspace_layout(a.n, a.lq, a.h, a.d);
   if ((rc = check_workspace(workspace, workspace_bytes, w))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

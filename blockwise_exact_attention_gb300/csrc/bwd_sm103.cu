@@ -49,6 +49,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "launch_cache.cuh"
 #include "ptx.cuh"
 
 namespace bea {
@@ -716,14 +717,25 @@ cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const C
   const int nkb = (a.lk + kBN - 1) / kBN;
   const long long blocks = (long long)nkb * a.n * a.hkv;
   if (blocks == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // Once per device context: allow the dynamic shared memory and read the
+  // register count. The register split is only sound at exactly kRegsLaunch
+  // registers per thread; refuse to launch otherwise (setmaxnreg.inc would
+  // never return).
+  static PerContext<int> regs_cache;
+  int regs = 0;
+  cudaError_t e = regs_cache.get(
+      [](int* v) {
+        cudaError_t r =
+            cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (r != cudaSuccess) return r;
+        cudaFuncAttributes fa;
+        r = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D>);
+        *v = fa.numRegs;
+        return r;
+      },
+      &regs);
   if (e != cudaSuccess) return e;
-  // The register split is only sound at exactly kRegsLaunch registers per
-  // thread; refuse to launch otherwise (setmaxnreg.inc would never return).
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const float scale_log2 = a.scale * 1.4426950408889634f;
   bwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p, scale_log2);
   *nlaunch += 1;
@@ -732,17 +744,15 @@ cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const C
 
 }  // namespace
 
-// One wave of resident CTAs of a row kernel over `rows` rows of D values.
+// One wave of resident CTAs of a row kernel over `rows` rows of D values
+// (`cache`: the kernel's wave size, looked up once per device context).
 template <typename K>
-cudaError_t row_grid(K kern, int64_t rows, int d, unsigned* grid) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, 0)) != cudaSuccess) return e;
+cudaError_t row_grid(PerContext<int>& cache, K kern, int64_t rows, int d, unsigned* grid) {
+  int cap = 0;
+  cudaError_t e = wave_cap(cache, kern, kRowThreads, 0, &cap);
+  if (e != cudaSuccess) return e;
   const int64_t rows_per_block = (int64_t)kRowThreads / (d / 8) * 2;
-  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
   *grid = (unsigned)(blocks < cap ? blocks : cap);
   return cudaSuccess;
 }
@@ -750,9 +760,11 @@ cudaError_t row_grid(K kern, int64_t rows, int d, unsigned* grid) {
 cudaError_t launch_bwd_prepare(const BwdParams& p, cudaStream_t s, int* nlaunch) {
   const int64_t rows = (int64_t)p.a.n * p.a.h * p.lq_pad;
   if (rows == 0) return cudaSuccess;
-  auto kern = (p.a.d == 128) ? bwd_preprocess_kernel<128> : bwd_preprocess_kernel<64>;
+  static PerContext<int> cap128, cap64;
+  const bool d128 = p.a.d == 128;
+  auto kern = d128 ? bwd_preprocess_kernel<128> : bwd_preprocess_kernel<64>;
   unsigned grid = 0;
-  cudaError_t e = row_grid(kern, rows, p.a.d, &grid);
+  cudaError_t e = row_grid(d128 ? cap128 : cap64, kern, rows, p.a.d, &grid);
   if (e != cudaSuccess) return e;
   kern<<<grid, kRowThreads, 0, s>>>(p);
   *nlaunch += 1;
@@ -769,10 +781,12 @@ cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUt
 cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch) {
   const int64_t groups = (int64_t)p.a.n * p.a.h * ((p.a.lq + 3) / 4);
   if (groups == 0) return cudaSuccess;
-  auto kern = (p.a.d == 128) ? bwd_convert_dq_kernel<128> : bwd_convert_dq_kernel<64>;
+  static PerContext<int> cap128, cap64;
+  const bool d128 = p.a.d == 128;
+  auto kern = d128 ? bwd_convert_dq_kernel<128> : bwd_convert_dq_kernel<64>;
   unsigned grid = 0;
   // row_grid counts two rows per thread group and pass; the convert takes one group of four
-  cudaError_t e = row_grid(kern, 2 * groups, p.a.d, &grid);
+  cudaError_t e = row_grid(d128 ? cap128 : cap64, kern, 2 * groups, p.a.d, &grid);
   if (e != cudaSuccess) return e;
   kern<<<grid, kRowThreads, 0, s>>>(p);
   *nlaunch += 1;

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "launch_cache.cuh"
 #include "ptx.cuh"
 
 namespace bea {
@@ -576,15 +577,25 @@ template <int D, bool kMerge>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t s, int* nlaunch) {
   using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  // Once per device context: allow the kernel's dynamic shared memory and read
+  // its register count. The register split above is only sound at exactly
+  // kRegsLaunch registers per thread; refuse to launch otherwise
+  // (setmaxnreg.inc would never return).
+  static PerContext<int> regs_cache;
+  int regs = 0;
+  cudaError_t e = regs_cache.get(
+      [](int* v) {
+        cudaError_t r = cudaFuncSetAttribute(fwd_bf16_kernel<D, kMerge>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (r != cudaSuccess) return r;
+        cudaFuncAttributes fa;
+        r = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D, kMerge>);
+        *v = fa.numRegs;
+        return r;
+      },
+      &regs);
   if (e != cudaSuccess) return e;
-  // The register split above is only sound at exactly kRegsLaunch registers
-  // per thread; refuse to launch otherwise (setmaxnreg.inc would never return).
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D, kMerge>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const int nqb = (p.a.lq + kSub * kBlockM - 1) / (kSub * kBlockM);
   const long long blocks = (long long)nqb * p.a.n * p.a.h;
   if (blocks == 0) return cudaSuccess;

@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "launch_cache.cuh"
 
 namespace bea {
 namespace {
@@ -128,17 +129,14 @@ cudaError_t launch_ring_merge(const MergeParams& p, cudaStream_t s, int* nlaunch
   const int64_t nrows = (int64_t)p.n * p.h * p.l;
   if (nrows == 0) return cudaSuccess;
   const int rows_per_block = kMergeThreads / (p.d >> 3) * kRowsInFlight;
-  int dev = 0, sms = 0;
-  cudaError_t e;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const bool f32 = p.blk_is_f32 != 0, fin = p.fin.ptr != nullptr;
   auto kern = f32 ? (fin ? ring_merge_kernel<true, true> : ring_merge_kernel<true, false>)
                   : (fin ? ring_merge_kernel<false, true> : ring_merge_kernel<false, false>);
-  int per_sm = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMergeThreads, 0)) != cudaSuccess) return e;
+  static PerContext<int> caps[4];  // one wave of resident blocks, per kernel variant and device context
+  int cap = 0;
+  const cudaError_t e = wave_cap(caps[(f32 ? 2 : 0) + (fin ? 1 : 0)], kern, kMergeThreads, 0, &cap);
+  if (e != cudaSuccess) return e;
   int64_t blocks = (nrows + rows_per_block - 1) / rows_per_block;
-  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);  // one wave of resident blocks
   if (blocks > cap) blocks = cap;
   kern<<<(unsigned)blocks, kMergeThreads, 0, s>>>(p);
   *nlaunch += 1;

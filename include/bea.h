@@ -222,13 +222,17 @@ int bea_flash_mha_bwd_finish(const bea_tensor* dq, float softmax_scale, int accu
  * library's own device memory; every GPU that loads the library holds that
  * array until the process exits. This call allocates nothing.
  *
- * Arguments and results are those of bea_flash_mha_bwd. A problem whose
- * workspace (bea_flash_mha_bwd_workspace_size) exceeds the array returns
- * BEA_ERR_WORKSPACE before anything is launched.
+ * Arguments and results are those of bea_flash_mha_bwd, checked in the same
+ * order and with the same error codes. Only a call that passes those checks
+ * and whose workspace (bea_flash_mha_bwd_workspace_size, computed without
+ * overflow) exceeds the array returns BEA_ERR_WORKSPACE, before anything is
+ * launched.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current and caches it; make that
- * first call before any stream capture. All calls on a device share the one
+ * The first call in a device's context looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it for that
+ * context; a new context on the device (e.g. after cudaDeviceReset) looks it
+ * up again on its first call. Make that first call before any stream
+ * capture. All calls on a device share the one
  * array, so two calls whose kernels may overlap on the GPU (different
  * streams, or several host threads) race on it: order them on one stream.
  * The array keeps the last call's contents; each call rewrites all of it

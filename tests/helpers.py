@@ -2,18 +2,36 @@
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 # Tolerances (stated against the fp64 oracle):
-#   bf16 out/dq/dk/dv: max-abs <= 2e-2; an element whose reference is so large
-#   that rounding the result itself to bf16 costs more (|ref| >= 4) may add
-#   half a bf16 ulp of |ref| — the final cast alone can be that far off.
+#   bf16 out/dq/dk/dv: max-abs <= 2e-2 on every element whose reference has
+#   |ref| < 4. Only where the result itself is a bf16 tensor AND |ref| >= 4
+#   may an element add half a bf16 ulp of |ref| to the bound: rounding the
+#   result to bf16 alone can cost that much there (half an ulp is 0.0156 at
+#   4 <= |ref| < 8). Elements that pass only because of that allowance are
+#   counted, and the count is printed with the largest such |ref|.
 #   lse: abs <= 1e-3. fp32 path: <= 1e-4 on all outputs. Ring vs single call
 #   (both fp32 outputs): <= 1e-3.
 TOL_BF16 = 2e-2
 TOL_LSE = 1e-3
 TOL_F32 = 1e-4
 TOL_RING = 1e-3
+ALLOWANCE_MIN_REF = 4.0
+
+# One record per bf16 comparison: (test-supplied name, elements compared,
+# elements that needed the rounding allowance, largest |ref| among them).
+# tests/conftest.py prints them in the session summary.
+ALLOWANCE_LOG: list = []
+# Free-form lines a test wants in the session summary (e.g. measured error margins).
+REPORT_LINES: list = []
+
+
+def report(line: str) -> None:
+    print(line)
+    REPORT_LINES.append(line)
 
 
 def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
@@ -22,13 +40,30 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def assert_close_bf16(got: np.ndarray, ref: np.ndarray, name: str, output_is_bf16: bool = True):
-    err = np.abs(got.astype(np.float64) - ref)
-    bound = TOL_BF16 + (bf16_half_ulp(ref) if output_is_bf16 else 0.0)
-    bad = err > bound
-    assert not bad.any(), (
-        f"{name}: {int(bad.sum())} elements out of tolerance; max err {err.max():.3e} "
-        f"at ref {ref.ravel()[np.argmax(err)]:.3e}")
-    return float(err.max())
+    """max |got - ref| <= 2e-2, plus half a bf16 ulp of |ref| only for bf16
+    results where |ref| >= 4. Prints how many elements needed that allowance."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    if output_is_bf16:
+        allowance = np.where(np.abs(ref) >= ALLOWANCE_MIN_REF, bf16_half_ulp(ref), 0.0)
+    else:
+        allowance = np.zeros_like(ref)
+    bad = ~(err <= TOL_BF16 + allowance)
+    if bad.any():
+        e = np.where(np.isnan(err), np.inf, err)
+        raise AssertionError(f"{name}: {int(bad.sum())} elements out of tolerance; max err {e.max():.3e} "
+                             f"at ref {ref.ravel()[np.argmax(e)]:.3e}")
+    needed = err > TOL_BF16
+    n_needed = int(needed.sum())
+    max_ref = float(np.abs(ref[needed]).max()) if n_needed else 0.0
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    ALLOWANCE_LOG.append((f"{test} {name}".strip(), int(err.size), n_needed, max_ref, float(err.max(initial=0.0))))
+    if n_needed:
+        print(f"[tolerance] {name}: {n_needed} of {err.size} elements pass only by the bf16 rounding "
+              f"allowance (|ref| >= {ALLOWANCE_MIN_REF:g}); largest such |ref| {max_ref:.3f}, "
+              f"largest err {err[needed].max():.3e}")
+    return float(err.max(initial=0.0))
 
 
 def assert_close(got: np.ndarray, ref: np.ndarray, tol: float, name: str):

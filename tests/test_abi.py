@@ -205,3 +205,43 @@ def test_selftest_argument_range(lib):
     assert lib.bea_selftest_inject_abort(-2) == ARG
     assert lib.bea_selftest_inject_abort(3) == 0     # armed (one-shot) ...
     assert lib.bea_selftest_inject_abort(-1) == 0    # ... and disarmed again before any launch
+
+
+def _bwd_args(n=1, l=256, h=4, hkv=2, d=128, dt=BF16, gdt=F32):
+    q, k, v, o, lse = good(n=n, l=l, h=h, hkv=hkv, d=d, dt=dt)
+    do = T([n, l, h, d], dt)
+    return [do, q, k, v, o, lse, T([n, l, h, d], gdt), T([n, l, hkv, d], gdt), T([n, l, hkv, d], gdt)]
+
+
+def noalloc(lib, args, scale=0.125, causal=1, wl=-1, wr=-1, acc=0):
+    r = ctypes.byref
+    return lib.bea_flash_mha_bwd_noalloc(*[r(a) if a is not None else None for a in args], scale, causal, wl, wr,
+                                         acc, None)
+
+
+def test_noalloc_checks_arguments_before_its_size(lib):
+    """A malformed call gets the error bea_flash_mha_bwd would give, not the array-size error,
+    even when its (malformed) shape would need more workspace than the array holds."""
+    big = 1 << 20  # needs ~2 GiB of workspace at h = 4, d = 128
+    args = _bwd_args(l=big)
+    args[0] = None                                      # dout missing
+    assert noalloc(lib, args) == ARG
+    args = _bwd_args(l=big)
+    args[6] = T([1, big, 4, 64], F32)                   # dq of the wrong shape
+    assert noalloc(lib, args) == SHAPE
+    assert noalloc(lib, _bwd_args(l=big), scale=-1.0) == ARG
+    assert noalloc(lib, _bwd_args(l=big, gdt=BF16), acc=1) == DTYPE
+    assert noalloc(lib, _bwd_args(l=big, h=4, hkv=3)) == SHAPE
+    # well-formed but too large for the array: only now the size error
+    assert noalloc(lib, _bwd_args(l=big)) == WS
+
+
+def test_workspace_size_saturates(lib):
+    huge = (1 << 31) - 1
+    assert lib.bea_flash_mha_bwd_workspace_size(huge, huge, huge, 128) == (1 << 64) - 1
+    assert lib.bea_flash_mha_bwd_workspace_size(1, 8192, 32, 128) == (
+        1 * 32 * 8192 * 128 * 4 + 2 * 32 * 8192 * 4)
+    # a tensor whose element count overflows 64 bits is rejected, not wrapped
+    args = _bwd_args()
+    args[1] = T([huge, huge, huge, 128], BF16, strides=[16, 16, 16, 1])
+    assert noalloc(lib, args) != OK

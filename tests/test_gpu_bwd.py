@@ -5,7 +5,8 @@ to the uploaded bf16, lse to fp32), never the GPU's, and the oracle backward
 consumes exactly those uploaded bits. Small cases span several tiles, a
 ragged tail, every mask mode, GQA, both head dims and lq != lk; the full-size
 workloads are checked on a subset of heads (all rows of those heads), with the
-other heads given inputs whose gradients are exactly zero.
+other heads given inputs whose gradients are exactly zero; the GPU forward is
+checked on every row of the same heads against the oracle forward.
 """
 
 import math
@@ -16,7 +17,7 @@ import pytest
 import oracle
 from blockwise_exact_attention_gb300 import workloads
 
-from helpers import assert_close_bf16, cached_inputs, to_dev, to_np
+from helpers import TOL_LSE, assert_close, assert_close_bf16, cached_inputs, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -155,14 +156,21 @@ def test_bwd_full_size_head_subset(name):
     out_full[:, :, hqs] = out_sub
     lse_full[:, hqs] = lse_sub
     q, k, v, do = (to_dev(x[s], torch.bfloat16) for s in ("q", "k", "v", "dout"))
+    hidx = torch.tensor(hqs, device="cuda")
+    kidx = torch.tensor(kvs, device="cuda")
+    # the GPU forward on every row of these query heads, against the oracle forward just computed
+    fo, fl = bea.flash_mha_fwd(q, k, v, w.softmax_scale, w.is_causal, w.window)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    assert_close_bf16(to_np(fo.index_select(2, hidx)), ro, "fwd out (whole heads)")
+    assert_close(to_np(fl.index_select(1, hidx)), rl, TOL_LSE, "fwd lse (whole heads)")
+    del fo, fl
     dq, dk, dv = bea.flash_mha_bwd(do, q, k, v, to_dev(out_full, torch.bfloat16), to_dev(lse_full, torch.float32),
                                    w.softmax_scale, w.is_causal, w.window, grad_dtype=torch.float32)
     torch.cuda.synchronize()
     assert bea.device_status() == 0
     rdq, rdk, rdv = oracle.attention_bwd(sub["dout"], sub["q"], sub["k"], sub["v"], out_sub, lse_sub,
                                          w.softmax_scale, w.is_causal, w.window)
-    hidx = torch.tensor(hqs, device="cuda")
-    kidx = torch.tensor(kvs, device="cuda")
     assert_close_bf16(to_np(dq.index_select(2, hidx)), rdq, "dq", output_is_bf16=False)
     assert_close_bf16(to_np(dk.index_select(2, kidx)), rdk, "dk", output_is_bf16=False)
     assert_close_bf16(to_np(dv.index_select(2, kidx)), rdv, "dv", output_is_bf16=False)

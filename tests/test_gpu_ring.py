@@ -11,7 +11,7 @@ import pytest
 import oracle
 from blockwise_exact_attention_gb300 import workloads
 
-from helpers import TOL_LSE, TOL_RING, assert_close, assert_close_bf16, cached_inputs, to_dev, to_np
+from helpers import TOL_LSE, TOL_RING, assert_close, assert_close_bf16, cached_inputs, report, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -74,7 +74,18 @@ def test_ring_full_size():
     assert bea.launches_since_reset(reset=True) == 8 + 7
     so32, sl32 = bea.flash_mha_fwd(q, k, v, s, True, out_dtype=torch.float32)
     torch.cuda.synchronize()
-    assert_close(to_np(ro32), to_np(so32), TOL_RING, "ring vs single out (fp32)")
+    # both sides against the oracle on sampled rows, reported next to their difference: the two
+    # round P to bf16 under different running maxima, so each carries its own rounding error
+    rows = np.array([0, 1, 2047, 2048, 2049, 4095, 6000, 8191, 8192, 12000, 14336, 16383])
+    oo, ol = oracle.attention_fwd(x["q"], x["k"], x["v"], s, True, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    e_ring = assert_close_bf16(to_np(ro32.index_select(1, idx)), oo, "ring out (fp32) vs oracle", output_is_bf16=False)
+    e_single = assert_close_bf16(to_np(so32.index_select(1, idx)), oo, "single out (fp32) vs oracle",
+                                 output_is_bf16=False)
+    diff_rows = float((ro32.index_select(1, idx) - so32.index_select(1, idx)).abs().max())
+    diff = assert_close(to_np(ro32), to_np(so32), TOL_RING, "ring vs single out (fp32)")
+    report(f"[ring 16k] max |ring - single| {diff:.3e} over all rows ({diff_rows:.3e} on the sampled rows); "
+          f"on the sampled rows ring vs oracle {e_ring:.3e}, single vs oracle {e_single:.3e}")
     assert_close(to_np(rl32), to_np(sl32), TOL_RING, "ring vs single lse")
     fo32, fl32 = bea.ring_attention_fwd(q, k, v, w.ring_chunks, s, True, out_dtype=torch.float32, fused=True)
     torch.cuda.synchronize()
@@ -92,9 +103,6 @@ def test_ring_full_size():
     torch.cuda.synchronize()
     assert float(np.abs(to_np(rob) - to_np(sob)).max()) <= 2e-2
     # sampled rows against the oracle
-    rows = np.array([0, 2047, 2048, 4095, 8191, 12000, 16383])
-    oo, ol = oracle.attention_fwd(x["q"], x["k"], x["v"], s, True, rows=rows)
-    idx = torch.from_numpy(rows).cuda()
     assert_close_bf16(to_np(rob.index_select(1, idx)), oo, "ring out")
     assert_close(to_np(rlb.index_select(2, idx)), ol, TOL_LSE, "ring lse")
     # backward: chunk pairs against one call, from the same (fp32) out/lse
