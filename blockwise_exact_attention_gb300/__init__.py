@@ -10,7 +10,8 @@ Public API (all calls run in libbea.so's CUDA kernels on the current stream):
 * ``flash_mha_fwd_merge(q, k, v, out_acc, lse_acc, ...)``: the fused ring
   step (a block's forward folded into the accumulator)
 * ``ring_attention_fwd / ring_attention_bwd``: ring attention replayed as
-  chunk steps on one GPU.
+  chunk steps on one GPU (``ring_attention_fwd_steps / ring_attention_bwd_steps``:
+  the library's one-call form of the same replay).
 * ``flash_attention / ring_attention``: the same as torch.autograd functions
   (the backward recomputed from the saved log-sum-exp).
 
@@ -26,6 +27,9 @@ from .ops import (  # noqa: F401
     flash_mha_fwd,
     flash_mha_fwd_merge,
     launches_since_reset,
+    ring_attention_bwd_steps,
+    ring_attention_fwd_steps,
+    ring_bwd_workspace_bytes,
     ring_merge,
     selftest_wait_timeout,
     selftest_inject_abort,

@@ -46,6 +46,9 @@ EXPORTS = (
     "bea_flash_mha_bwd_prepare",
     "bea_flash_mha_bwd_kv_block",
     "bea_flash_mha_bwd_finish",
+    "bea_ring_attention_fwd",
+    "bea_ring_attention_bwd_workspace_size",
+    "bea_ring_attention_bwd",
 )
 
 
@@ -109,6 +112,12 @@ def load() -> ctypes.CDLL:
     lib.bea_flash_mha_bwd_kv_block.restype = i
     lib.bea_flash_mha_bwd_finish.argtypes = [P, f, i, vp, sz, vp]
     lib.bea_flash_mha_bwd_finish.restype = i
+    lib.bea_ring_attention_fwd.argtypes = [P, P, P, P, P, P, i, f, i, i, i, vp]
+    lib.bea_ring_attention_fwd.restype = i
+    lib.bea_ring_attention_bwd_workspace_size.argtypes = [i64, i64, i64, i64, i]
+    lib.bea_ring_attention_bwd_workspace_size.restype = sz
+    lib.bea_ring_attention_bwd.argtypes = [P, P, P, P, P, P, P, P, P, i, f, i, i, i, vp, sz, vp]
+    lib.bea_ring_attention_bwd.restype = i
     _LIB = lib
     return lib
 

@@ -13,15 +13,13 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/bea.h"
+#include "abi_internal.h"
 #include "common.cuh"
 #include "launch_cache.cuh"
 #include "status.cuh"
 
-namespace {
-
-using bea::AttnDims;
-using bea::Lse3;
-using bea::Seq4;
+namespace bea {
+namespace abi {
 
 thread_local int g_last_launches = 0;
 
@@ -219,9 +217,6 @@ int finish(cudaError_t e, int launches) {
 }
 
 // Workspace layout of the backward: [dq_acc | D | lse2], each 256-byte aligned.
-struct BwdWorkspace {
-  size_t dq_off, d_off, l_off, total;
-};
 // Byte sizes saturate at SIZE_MAX instead of wrapping: a size no buffer can
 // have, which check_workspace then rejects.
 size_t mul_sat(size_t a, size_t b) {
@@ -252,7 +247,7 @@ int check_workspace(const void* workspace, size_t workspace_bytes, const BwdWork
 }
 
 // Workspace pointers of the bf16 backward stages.
-void set_workspace(bea::BwdParams* p, void* workspace, const BwdWorkspace& w) {
+void set_workspace(BwdParams* p, void* workspace, const BwdWorkspace& w) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p->dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
   p->d_row = reinterpret_cast<float*>(ws + w.d_off);
@@ -300,9 +295,9 @@ int query_side_dims(const bea_tensor* t, AttnDims* a) {
   return BEA_OK;
 }
 
-}  // namespace
+}  // namespace abi
 
-namespace bea {
+using namespace abi;
 
 unsigned long long current_context_id() {
   std::call_once(g_ctx_fn_once, load_ctx_fns);
@@ -338,6 +333,10 @@ cudaError_t device_sm_count(int* sms) {
 }
 
 }  // namespace bea
+
+using namespace bea::abi;
+using bea::AttnDims;
+using bea::Seq4;
 
 extern "C" {
 
@@ -422,6 +421,8 @@ int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_
   p.lse = lse3(lse_acc);
   p.merge = 1;
   p.fin = out_final ? seq4(out_final) : Seq4{nullptr, 0, 0, 0};
+  p.fin_b0 = 0;
+  p.fin_b1 = a.n;
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
   p.inject_abort = take_inject_abort();
   CUtensorMap tq, tk, tv;
@@ -462,6 +463,7 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
     return finish(bea::launch_bwd_f32(p, s, &launches), launches);
   }
   bea::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
   p.a = a;
   p.dout = seq4(dout);
   p.out = seq4(out);

@@ -85,6 +85,9 @@ constexpr int kMmaWarp = 13;
 // so the wait costs them nothing.
 constexpr uint32_t kReadyBar = 1;
 constexpr uint32_t kReadyThreads = 256 + 32;
+// dK / dV epilogue of key warpgroup c: its 128 threads hand the staged chunk to one
+// another over named barrier kEpiBar + c (every thread joins every phase, with or without work).
+constexpr uint32_t kEpiBar = 3;
 
 template <int D>
 struct BwdCfg {
@@ -341,16 +344,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   // ---- work: key blocks in ascending order (under a causal mask the first see the most queries) ----
-  // Without a mask band every CTA has the same work. With one query head per K/V head the
+  // When the band covers every (query, key) pair (no mask, or a ring step's chunk pair that
+  // lies wholly inside it) every CTA has the same work. With one query head per K/V head the
   // CTAs are then taken head by head, so that the ones running together share one head's
   // Q/dO tiles and dQ accumulator rows in L2 (measured: 32k d=64 full attention -12%, 8k d=128
-  // -6%). Under a causal or window band the key blocks go in ascending order (longest first),
-  // and so do grouped heads (their 4x longer CTAs measured 3% slower head by head).
-  const int nkv = a.n * a.hkv;
+  // -6%; the 16k ring's full chunk pairs, run as a batch of 7 chunks x 16 heads, would otherwise
+  // spread ~150 heads' Q/dO/dQ over L2). Under a causal or window band the batches go one
+  // after another and, within one, the key blocks in ascending order (longest first) with the
+  // K/V heads fastest; so do grouped heads (their 4x longer CTAs measured 3% slower head by head).
   const int nkb = (a.lk + kBN - 1) / kBN;
-  const bool head_major = a.wl >= kUnbounded && a.wr >= kUnbounded && a.h == a.hkv;
-  const int kb = head_major ? (int)(blockIdx.x % nkb) : (int)(blockIdx.x / nkv);
-  const int bkv = head_major ? (int)(blockIdx.x / nkb) : (int)(blockIdx.x % nkv);
+  const bool full_band = a.wl >= a.lq - 1 && a.wr >= a.lk - 1;
+  const bool head_major = full_band && a.h == a.hkv;
+  const int per_batch = nkb * a.hkv;
+  const int kb = head_major ? (int)(blockIdx.x % nkb) : (int)((blockIdx.x % per_batch) / a.hkv);
+  const int bkv = head_major ? (int)(blockIdx.x / nkb)
+                             : (int)(blockIdx.x / per_batch) * a.hkv + (int)(blockIdx.x % a.hkv);
   const int b = bkv / a.hkv;
   const int kvh = bkv % a.hkv;
   BwdSched sc;
@@ -392,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the next kernel on the stream may start as soon as every CTA of this one is running
+  grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   // TMEM slot h: S_h^T at 128h (then P^T / dS^T, 16 + 16 columns per key warpgroup), dP_h^T / dQ_h^T at 128h + 64
   const uint32_t T_DP = 64, T_DV = 256, T_DK = 384;
@@ -410,11 +420,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem + C::kKOff + x * 16384, &tk, kv_full, x * 64, kvh, sc.k0, b);
         tma_load_4d(smem + C::kVOff + x * 16384, &tv, kv_full, x * 64, kvh, sc.k0, b);
       }
+      // With accumulate, the epilogue reads this CTA's dK and dV rows before adding to them.
+      // Have L2 fetch them a few rows per iteration, spread over the main loop, so that the
+      // epilogues of a wave's CTAs (which end together) do not all read HBM at once.
+      const int pf_per_it = p.accumulate ? (kBN + sc.n_iter - 1) / sc.n_iter : 0;
       int it = 0;
       for (; it < sc.n_iter; ++it) {
         const int s = it & 1;
         const int hq = kvh * sc.g + it / nt;
         const int q0 = (sc.i_lo + it % nt) * kBM;
+        for (int rr = it * pf_per_it; rr < min((it + 1) * pf_per_it, kBN); ++rr) {
+          const int key = sc.k0 + rr;
+          if (key < a.lk) {
+            bulk_prefetch_l2(reinterpret_cast<const float*>(p.dk.ptr) + b * p.dk.sn + (int64_t)key * p.dk.sl +
+                                 kvh * p.dk.sh,
+                             D * 4);
+            bulk_prefetch_l2(reinterpret_cast<const float*>(p.dv.ptr) + b * p.dv.sn + (int64_t)key * p.dv.sl +
+                                 kvh * p.dv.sh,
+                             D * 4);
+          }
+        }
         if (it >= 2 && !wait_parity(&qdo_empty[s], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&q_full[s], C::kTileBytes + 2 * kBM * 4);
         for (int x = 0; x < C::kBoxes; ++x)
@@ -608,57 +633,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---- dK / dV epilogue: key warpgroup 0 writes dV, warpgroup 1 writes dK ----
+    // Through shared memory, as the forward's epilogue: each key thread writes 32 fp32 values
+    // of its row (128 bytes, 16-byte pieces of row j rotated by j & 7) into a staging chunk,
+    // then the warpgroup's 128 threads move the chunk as 16-byte pieces, 8 threads per row
+    // segment, so that the accumulate read-modify-write and the stores cover whole 128-byte
+    // segments. The staging buffers are the Q (dV) and dO (dK) stages, free once dkv_full says
+    // every MMA has completed (never loaded when the CTA saw no query tile).
     if (ok && sc.n_iter > 0) ok = warp_wait_parity(dkv_full, 0, abort_flag, p.status);
-    if (ok) {
+    // a dependent launch (the next ring step) adds into dK / dV only after the launch before it is done
+    grid_dependency_wait();
+    {
       tc_fence_after();
       const bool have = sc.n_iter > 0;
       const float mul = c ? a.scale : 1.f;
       const bool f32 = c ? p.dk_is_f32 : p.dv_is_f32;
-      const int64_t off0 = c ? (b * p.dk.sn + (int64_t)kj * p.dk.sl + kvh * p.dk.sh)
-                             : (b * p.dv.sn + (int64_t)kj * p.dv.sl + kvh * p.dv.sh);
-      void* base = c ? p.dk.ptr : p.dv.ptr;
+      const Seq4 dst = c ? p.dk : p.dv;
+      uint8_t* stage = smem + (c ? C::kDOOff : C::kQOff);
       const uint32_t src_t = tmem + lane_base + (c ? T_DK : T_DV);
+      const int piece = j & 7;
+      const uint32_t ep_id = kEpiBar + c;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t src[32];
-        if (have) {
-          tmem_ld32(src_t + c0, src);
-          tmem_wait_ld();
-          reg_fence<32>(src);
-        } else {
+        if (ok) {
+          uint32_t src[32];
+          if (have) {
+            tmem_ld32(src_t + c0, src);
+            tmem_wait_ld();
+            reg_fence<32>(src);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) src[e] = 0u;
+            for (int e = 0; e < 32; ++e) src[e] = 0u;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(stage + j * 128 + ((k ^ (j & 7)) * 16)) =
+                make_float4(__uint_as_float(src[4 * k]) * mul, __uint_as_float(src[4 * k + 1]) * mul,
+                            __uint_as_float(src[4 * k + 2]) * mul, __uint_as_float(src[4 * k + 3]) * mul);
         }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) src[e] = __float_as_uint(__uint_as_float(src[e]) * mul);
-        if (kj >= a.lk) continue;  // ragged last key block: the loads above stay warp-wide
-        if (f32) {
-          float* dst = reinterpret_cast<float*>(base) + off0 + c0;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float4 v4 = make_float4(__uint_as_float(src[e]), __uint_as_float(src[e + 1]),
-                                    __uint_as_float(src[e + 2]), __uint_as_float(src[e + 3]));
+        named_bar_sync(ep_id, 128);
+        if (ok) {
+          if (f32) {
+            // L2-only loads (.cg): a previous ring step may have written these rows from another SM
+            float4 old4[8];
             if (p.accumulate) {
-              const float4 o = *reinterpret_cast<const float4*>(dst + e);
-              v4.x += o.x;
-              v4.y += o.y;
-              v4.z += o.z;
-              v4.w += o.w;
-            }
-            *reinterpret_cast<float4*>(dst + e) = v4;
-          }
-        } else {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + off0 + c0;
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v4;
-            v4.x = pack_bf16x2(__uint_as_float(src[e]), __uint_as_float(src[e + 1]));
-            v4.y = pack_bf16x2(__uint_as_float(src[e + 2]), __uint_as_float(src[e + 3]));
-            v4.z = pack_bf16x2(__uint_as_float(src[e + 4]), __uint_as_float(src[e + 5]));
-            v4.w = pack_bf16x2(__uint_as_float(src[e + 6]), __uint_as_float(src[e + 7]));
-            *reinterpret_cast<uint4*>(dst + e) = v4;
+              for (int k = 0; k < 8; ++k) {
+                const int row = (j >> 3) + 16 * k;
+                const int key = sc.k0 + row;
+                if (key < a.lk)
+                  old4[k] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(dst.ptr) +
+                                                                   b * dst.sn + (int64_t)key * dst.sl +
+                                                                   kvh * dst.sh + c0 + 4 * piece));
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int row = (j >> 3) + 16 * k;
+              const int key = sc.k0 + row;
+              if (key >= a.lk) continue;  // ragged last key block
+              float4 v4 = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
+              if (p.accumulate) {
+                v4.x += old4[k].x;
+                v4.y += old4[k].y;
+                v4.z += old4[k].z;
+                v4.w += old4[k].w;
+              }
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst.ptr) + b * dst.sn + (int64_t)key * dst.sl +
+                                         kvh * dst.sh + c0 + 4 * piece) = v4;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int row = (j >> 3) + 16 * k;
+              const int key = sc.k0 + row;
+              if (key >= a.lk) continue;
+              const float4 v4 = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
+              uint2 v2;
+              v2.x = pack_bf16x2(v4.x, v4.y);
+              v2.y = pack_bf16x2(v4.z, v4.w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dst.ptr) + b * dst.sn +
+                                        (int64_t)key * dst.sl + kvh * dst.sh + c0 + 4 * piece) = v2;
+            }
           }
         }
+        named_bar_sync(ep_id, 128);
       }
     }
   } else {
@@ -737,7 +795,18 @@ cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const C
   if (e != cudaSuccess) return e;
   if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  bwd_bf16_kernel<D><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p, scale_log2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, bwd_bf16_kernel<D>, tq, tk, tv, tdo, p, scale_log2);
+  if (e != cudaSuccess) return e;
   *nlaunch += 1;
   return cudaGetLastError();
 }

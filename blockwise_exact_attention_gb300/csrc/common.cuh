@@ -73,7 +73,10 @@ struct FwdParams {
   int out_is_f32;
   Lse3 lse;  // merge: the accumulator's log-sum-exp (read and written)
   int merge;  // fold the block into (out, lse) instead of writing it
+  int merge_init;  // merge only: the accumulator holds nothing yet ((0, -inf)): write the block, read nothing
   Seq4 fin;   // merge only: bf16 copy of the merged rows, ptr may be null
+  int fin_b0, fin_b1;  // merge only: fin is written for batch indices [fin_b0, fin_b1) only
+  int pdl;    // launch with programmatic stream serialisation (see grid_dependency_wait)
   uint32_t* status;
   int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at tile inject_abort - 1
 };
@@ -91,6 +94,7 @@ struct BwdParams {
   float* d_row;   // workspace: [n, h, lq_pad] D = rowsum(dO * O)
   float* lse2;    // workspace: [n, h, lq_pad] lse * log2(e), +inf for rows without keys / padding
   int lq_pad;
+  int pdl;        // launch with programmatic stream serialisation (see grid_dependency_wait)
   uint32_t* status;
   int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at iteration inject_abort - 1
 };

@@ -69,6 +69,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when th
 //    issues only after phase j.
 constexpr uint32_t kPReadyBar = 1;
 constexpr uint32_t kPReadyThreads = 128 + 32;
+// Epilogue of subtile t: its 128 softmax threads hand the staged O chunk to one
+// another over named barrier kEpiBar + t (every thread of the subtile joins
+// every phase, with or without work).
+constexpr uint32_t kEpiBar = 3;
 
 template <int D>
 struct FwdCfg {
@@ -80,7 +84,8 @@ struct FwdCfg {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1;
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
+  static constexpr int kEpiOff = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/;  // per-row merge weights
+  static constexpr int kSmemBytes = kEpiOff + kSub * 3 * kBlockM * 4 + 1024 /*align slack*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
   static constexpr uint32_t kVLbo = 64 * 128 * 2;  // byte distance of 64-column V blocks
@@ -139,13 +144,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work decomposition: longest (latest) query blocks first ----
   const int nqb = (a.lq + kSub * kBlockM - 1) / (kSub * kBlockM);
   const int bh_count = a.n * a.h;
-  // Without a mask band every CTA has the same work. With one query head per K/V head the
+  // When the band covers every (query, key) pair (no mask, or a ring step's chunk pair that
+  // lies wholly inside it) every CTA has the same work. With one query head per K/V head the
   // CTAs are then taken head by head, so that the ones running together stream one head's K/V
-  // tiles from L2 (measured: 32k d=64 full attention -2%). Under a causal or window band the
-  // latest (longest) query blocks go first.
-  const bool head_major = a.wl >= kUnbounded && a.wr >= kUnbounded && a.h == a.hkv;
-  const int qb = head_major ? nqb - 1 - (int)(blockIdx.x % nqb) : nqb - 1 - (int)(blockIdx.x / bh_count);
-  const int bh = head_major ? (int)(blockIdx.x / nqb) : (int)(blockIdx.x % bh_count);
+  // tiles from L2 (measured: 32k d=64 full attention -2%; the 16k ring's full chunk pairs, run
+  // as a batch of 7 chunks x 16 heads, would otherwise spread ~150 heads' K/V over L2).
+  // Under a causal or window band the batches go one after another and, within one, the
+  // latest (longest) query blocks first, the heads fastest.
+  const bool full_band = a.wl >= a.lq - 1 && a.wr >= a.lk - 1;
+  const bool head_major = full_band && a.h == a.hkv;
+  const int per_batch = nqb * a.h;
+  const int qb = head_major ? nqb - 1 - (int)(blockIdx.x % nqb)
+                            : nqb - 1 - (int)((blockIdx.x % per_batch) / a.h);
+  const int bh = head_major ? (int)(blockIdx.x / nqb)
+                            : (int)(blockIdx.x / per_batch) * a.h + (int)(blockIdx.x % a.h);
+  (void)bh_count;
   const int b = bh / a.h, hq = bh % a.h, kvh = hq / (a.h / a.hkv);
   Sched sc;
   sc.q0 = qb * kSub * kBlockM;
@@ -185,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the next kernel on the stream may start as soon as every CTA of this one is running
+  grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
@@ -209,6 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint64_t pol = l2_policy_evict_last();
+      // Fused ring step: the accumulator rows this CTA folds into are read only in the
+      // epilogue. Have L2 fetch them a few rows per K tile, spread over the main loop: all at
+      // once at the start would queue ahead of the first tiles' loads, and left to the epilogue
+      // the reads of every CTA of a wave (which all end together) would share HBM at once.
+      const int ntiles = sc.hi_all - sc.lo_all;
+      const bool pf = kMerge && !p.merge_init && ntiles > 0;
+      const int pf_per_tile = pf ? (kSub * kBlockM + ntiles - 1) / ntiles : 0;
       int it = 0;
       for (int j = sc.lo_all; j < sc.hi_all; ++j, ++it) {
         const int s = it % C::kStages;
@@ -219,6 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d_hint(kd + x * 16384, &tk, &k_full[s], x * 64, kvh, j * kBlockN, b, pol);
+        for (int rr = it * pf_per_tile; rr < min((it + 1) * pf_per_tile, kSub * kBlockM); ++rr) {
+          const int qrow = sc.q0 + rr;
+          if (qrow < a.lq)
+            bulk_prefetch_l2(reinterpret_cast<const float*>(p.out.ptr) + b * p.out.sn + (int64_t)qrow * p.out.sl +
+                                 hq * p.out.sh,
+                             D * 4);
+        }
       }
       // Loads still in flight must land before the CTA's shared memory goes away.
       const int issued = it;
@@ -459,107 +488,213 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(kPReadyBar + t, kPReadyThreads);
     }
     // ---- epilogue ----
+    // O leaves TMEM through shared memory so that global memory sees whole
+    // 128-byte row segments: each row's thread writes a chunk of its row (32
+    // fp32 or 64 bf16 values, 128 bytes) into a staging buffer with the 16-byte
+    // pieces of row r rotated by r & 7 (bank-conflict free both ways), then the
+    // subtile's 128 threads move the chunk as 16-byte pieces, 8 threads per
+    // row segment. The staging buffer is this subtile's Q tile, free once every
+    // S_t has completed, which o_full[t] implies (for a subtile without tiles Q_t
+    // was never loaded).
     const bool have_o = my_lo < my_hi;
+    const bool row_ok = qi < a.lq;
+    float* lse_p = p.lse.ptr + b * p.lse.sn + hq * p.lse.sh + qi;
+    // the coalesced phase: thread u of the subtile takes 16-byte piece u % 8 of rows u / 8 + 16 k
+    const int u = r;
+    const int piece = u & 7;
+    const bool init = kMerge && p.merge_init != 0;
+    // Fused ring step: this thread's accumulator pieces of 32 columns (L2-only loads, .cg: under
+    // a dependent launch the previous ring step wrote these rows from other SMs, and no L1 line
+    // of an earlier read may stand in for them).
+    float4 acc4[kMerge ? 8 : 1], accn[kMerge ? 8 : 1];
+    auto load_acc = [&](float4* dst4, int cc) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int qrow = qs + (u >> 3) + 16 * k;
+        if (!init && qrow < a.lq)
+          dst4[k] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out.ptr) +
+                                                           b * p.out.sn + (int64_t)qrow * p.out.sl + hq * p.out.sh +
+                                                           cc + 4 * piece));
+      }
+    };
+    float la = -INFINITY;
+    if constexpr (kMerge) {
+      if (qs < a.lq && !init) {
+        // Once the launch this one depends on (the previous ring step) is done, this row's
+        // log-sum-exp and this thread's first accumulator pieces are read while the last P V
+        // completes.
+        grid_dependency_wait();
+        if (row_ok) la = __ldcg(lse_p);
+        if (ok) load_acc(acc4, 0);
+      }
+    }
     if (ok && have_o) ok = warp_wait_parity(&o_full[t], 0, abort_flag, p.status);
-    if (ok && qs < a.lq) {
+    if (qs < a.lq) {  // uniform over the subtile: all 128 threads join the barriers below
+      // a dependent launch (the next ring step) touches out/lse only after the launch before it is done
+      grid_dependency_wait();
       tc_fence_after();
-      const bool row_ok = qi < a.lq;
       const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
       const float L = (l_sum > 0.f) ? (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f : -INFINITY;
-      float* lse_p = p.lse.ptr + b * p.lse.sn + hq * p.lse.sh + qi;
-      // Fused ring step: fold this block's (O, L) into the fp32 accumulator (out, lse) by the
-      // log-sum-exp merge of flash_attn_jax flash_sharding.py, "Ring Forward":
-      //   L' = max + log1p(exp(min - max)), acc <- acc exp(La - L') + O exp(L - L'),
-      // leaving a row whose two log-sum-exps are both -inf unchanged.
-      float wa = 0.f, wb = inv, l_new = L;
-      bool keep = false;
-      // merge: the whole accumulator row is loaded up front (its loads overlap one another
-      // instead of waiting chunk by chunk; the S registers are free by now)
-      float4 arow[kMerge ? D / 4 : 1];
-      float* acc_row = kMerge ? reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn + (int64_t)qi * p.out.sl +
-                                    hq * p.out.sh
-                              : nullptr;
+      uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+      float* rowv = reinterpret_cast<float*>(smem + C::kEpiOff) + t * 3 * kBlockM;  // per row: wa, wb, keep
+      const int ep_id = kEpiBar + t;
       if constexpr (kMerge) {
-        if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c) arow[c] = *reinterpret_cast<const float4*>(acc_row + 4 * c);
+        // Fused ring step: fold this block's (O, L) into the fp32 accumulator (out, lse) by the
+        // log-sum-exp merge of flash_attn_jax flash_sharding.py, "Ring Forward":
+        //   L' = max + log1p(exp(min - max)), acc <- acc exp(La - L') + O exp(L - L'),
+        // leaving a row whose two log-sum-exps are both -inf unchanged. The first step of a ring
+        // (merge_init) has nothing to fold into: acc <- O / l, lse <- L.
+        float wa = 0.f, wb = inv, l_new = L;
+        bool keep = false;
+        if (!init) {
+          const float mx = fmaxf(la, L);
+          if (mx == -INFINITY) {
+            keep = true;
+          } else {
+            const float mn = fminf(la, L);
+            l_new = mx + log1pf(expf(mn - mx));
+            wa = expf(la - l_new);
+            wb = expf(L - l_new) * inv;
+          }
         }
-        const float la = row_ok ? *lse_p : -INFINITY;
-        const float mx = fmaxf(la, L);
-        if (mx == -INFINITY) {
-          keep = true;
+        rowv[3 * r] = wa;
+        rowv[3 * r + 1] = wb;
+        rowv[3 * r + 2] = keep ? 1.f : 0.f;
+        if (ok && row_ok && !keep) *lse_p = l_new;
+        const bool fin_on = p.fin.ptr != nullptr && b >= p.fin_b0 && b < p.fin_b1;
+        // the next 32 columns' pieces are loaded while the current ones are combined
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          if (ok && c0 + 32 < D) load_acc(accn, c0 + 32);
+          if (ok) {
+            uint32_t orow[32];
+            if (have_o) {
+              tmem_ld32(o_tmem + c0, orow);
+              tmem_wait_ld();
+              reg_fence<32>(orow);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) orow[c] = 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(stage + r * 128 + ((k ^ (r & 7)) * 16)) =
+                  make_uint4(orow[4 * k], orow[4 * k + 1], orow[4 * k + 2], orow[4 * k + 3]);
+          }
+          named_bar_sync(ep_id, 128);
+          if (ok) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int row = (u >> 3) + 16 * k;
+              const int qrow = qs + row;
+              if (qrow >= a.lq) continue;
+              const float rwa = rowv[3 * row], rwb = rowv[3 * row + 1];
+              const bool rkeep = rowv[3 * row + 2] != 0.f;
+              const float4 o = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
+              float4 m;
+              if (init) {
+                m = make_float4(o.x * rwb, o.y * rwb, o.z * rwb, o.w * rwb);
+              } else if (rkeep) {
+                m = acc4[k];
+              } else {
+                m = make_float4(fmaf(o.x, rwb, acc4[k].x * rwa), fmaf(o.y, rwb, acc4[k].y * rwa),
+                                fmaf(o.z, rwb, acc4[k].z * rwa), fmaf(o.w, rwb, acc4[k].w * rwa));
+              }
+              if (!rkeep)
+                *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn +
+                                           (int64_t)qrow * p.out.sl + hq * p.out.sh + c0 + 4 * piece) = m;
+              if (fin_on) {
+                uint2 v2;
+                v2.x = pack_bf16x2(m.x, m.y);
+                v2.y = pack_bf16x2(m.z, m.w);
+                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.fin.ptr) + b * p.fin.sn +
+                                          (int64_t)qrow * p.fin.sl + hq * p.fin.sh + c0 + 4 * piece) = v2;
+              }
+            }
+          }
+          named_bar_sync(ep_id, 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc4[k] = accn[k];
+        }
+      } else {
+        if (ok && row_ok) *lse_p = L;
+        if (p.out_is_f32) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            if (ok) {
+              uint32_t orow[32];
+              if (have_o) {
+                tmem_ld32(o_tmem + c0, orow);
+                tmem_wait_ld();
+                reg_fence<32>(orow);
+              } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) orow[c] = 0u;
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float4*>(stage + r * 128 + ((k ^ (r & 7)) * 16)) =
+                    make_float4(__uint_as_float(orow[4 * k]) * inv, __uint_as_float(orow[4 * k + 1]) * inv,
+                                __uint_as_float(orow[4 * k + 2]) * inv, __uint_as_float(orow[4 * k + 3]) * inv);
+            }
+            named_bar_sync(ep_id, 128);
+            if (ok) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int row = (u >> 3) + 16 * k;
+                const int qrow = qs + row;
+                if (qrow >= a.lq) continue;
+                *reinterpret_cast<uint4*>(reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn +
+                                          (int64_t)qrow * p.out.sl + hq * p.out.sh + c0 + 4 * piece) =
+                    *reinterpret_cast<const uint4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
+              }
+            }
+            named_bar_sync(ep_id, 128);
+          }
         } else {
-          const float mn = fminf(la, L);
-          l_new = mx + log1pf(expf(mn - mx));
-          wa = expf(la - l_new);
-          wb = expf(L - l_new) * inv;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            if (ok) {
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                uint32_t orow[32];
+                if (have_o) {
+                  tmem_ld32(o_tmem + c0 + 32 * hf, orow);
+                  tmem_wait_ld();
+                  reg_fence<32>(orow);
+                } else {
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) orow[c] = 0u;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int e = 8 * k;
+                  uint4 v4;
+                  v4.x = pack_bf16x2(__uint_as_float(orow[e]) * inv, __uint_as_float(orow[e + 1]) * inv);
+                  v4.y = pack_bf16x2(__uint_as_float(orow[e + 2]) * inv, __uint_as_float(orow[e + 3]) * inv);
+                  v4.z = pack_bf16x2(__uint_as_float(orow[e + 4]) * inv, __uint_as_float(orow[e + 5]) * inv);
+                  v4.w = pack_bf16x2(__uint_as_float(orow[e + 6]) * inv, __uint_as_float(orow[e + 7]) * inv);
+                  const int kk = 4 * hf + k;
+                  *reinterpret_cast<uint4*>(stage + r * 128 + ((kk ^ (r & 7)) * 16)) = v4;
+                }
+              }
+            }
+            named_bar_sync(ep_id, 128);
+            if (ok) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int row = (u >> 3) + 16 * k;
+                const int qrow = qs + row;
+                if (qrow >= a.lq) continue;
+                *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out.ptr) + b * p.out.sn +
+                                          (int64_t)qrow * p.out.sl + hq * p.out.sh + c0 + 8 * piece) =
+                    *reinterpret_cast<const uint4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
+              }
+            }
+            named_bar_sync(ep_id, 128);
+          }
         }
       }
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t orow[32];
-        if (have_o) {
-          tmem_ld32(o_tmem + c0, orow);
-          tmem_wait_ld();
-          reg_fence<32>(orow);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) orow[c] = 0u;
-        }
-        if (!row_ok) continue;
-        if constexpr (kMerge) {
-          float* acc = acc_row + c0;
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            float4 a0 = arow[(c0 + c) / 4];
-            float4 a1 = arow[(c0 + c) / 4 + 1];
-            if (!keep) {
-              a0 = make_float4(fmaf(__uint_as_float(orow[c]), wb, a0.x * wa),
-                               fmaf(__uint_as_float(orow[c + 1]), wb, a0.y * wa),
-                               fmaf(__uint_as_float(orow[c + 2]), wb, a0.z * wa),
-                               fmaf(__uint_as_float(orow[c + 3]), wb, a0.w * wa));
-              a1 = make_float4(fmaf(__uint_as_float(orow[c + 4]), wb, a1.x * wa),
-                               fmaf(__uint_as_float(orow[c + 5]), wb, a1.y * wa),
-                               fmaf(__uint_as_float(orow[c + 6]), wb, a1.z * wa),
-                               fmaf(__uint_as_float(orow[c + 7]), wb, a1.w * wa));
-              *reinterpret_cast<float4*>(acc + c) = a0;
-              *reinterpret_cast<float4*>(acc + c + 4) = a1;
-            }
-            if (p.fin.ptr != nullptr) {
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.fin.ptr) + b * p.fin.sn +
-                                   (int64_t)qi * p.fin.sl + hq * p.fin.sh + c0 + c;
-              uint4 v4;
-              v4.x = pack_bf16x2(a0.x, a0.y);
-              v4.y = pack_bf16x2(a0.z, a0.w);
-              v4.z = pack_bf16x2(a1.x, a1.y);
-              v4.w = pack_bf16x2(a1.z, a1.w);
-              *reinterpret_cast<uint4*>(dst) = v4;
-            }
-          }
-        } else if (p.out_is_f32) {
-          float* dst = reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn + (int64_t)qi * p.out.sl +
-                       hq * p.out.sh + c0;
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const float4 v4 = make_float4(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv,
-                                          __uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
-            *reinterpret_cast<float4*>(dst + c) = v4;
-          }
-        } else {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out.ptr) + b * p.out.sn +
-                               (int64_t)qi * p.out.sl + hq * p.out.sh + c0;
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v4;
-            v4.x = pack_bf16x2(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv);
-            v4.y = pack_bf16x2(__uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
-            v4.z = pack_bf16x2(__uint_as_float(orow[c + 4]) * inv, __uint_as_float(orow[c + 5]) * inv);
-            v4.w = pack_bf16x2(__uint_as_float(orow[c + 6]) * inv, __uint_as_float(orow[c + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c) = v4;
-          }
-        }
-      }
-      if (row_ok && !keep) *lse_p = l_new;
     }
   }
 
@@ -600,7 +735,18 @@ cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtens
   const long long blocks = (long long)nqb * p.a.n * p.a.h;
   if (blocks == 0) return cudaSuccess;
   const float scale_log2 = p.a.scale * 1.4426950408889634f;
-  fwd_bf16_kernel<D, kMerge><<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, p, scale_log2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, fwd_bf16_kernel<D, kMerge>, tq, tk, tv, p, scale_log2);
+  if (e != cudaSuccess) return e;
   *nlaunch += 1;
   return cudaGetLastError();
 }

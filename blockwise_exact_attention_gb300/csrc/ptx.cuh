@@ -165,6 +165,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Bring `bytes` (a multiple of 16, 16-byte aligned address) of global memory
+// into L2 without waiting for it and without touching shared memory or L1.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream is still
+// running; it must call grid_dependency_wait() before it reads anything that
+// kernel writes or writes anything that kernel reads or writes. Both are
+// no-ops for a kernel launched the ordinary way.
+// This CTA lets the next kernel on the stream start (once every CTA has said so or exited).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the kernel(s) this launch depends on have completed and their writes are visible.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -196,6 +196,44 @@ def ring_merge(out_acc, lse_acc, out_blk, lse_blk, out_final=None):
     return out_acc, lse_acc
 
 
+def ring_attention_fwd_steps(q, k, v, out_acc, lse, n_chunks, softmax_scale=None, is_causal=False,
+                            window_size=(-1, -1), out_final=None):
+    """The whole ring forward replay in one library call: every live chunk pair folded
+    into the fp32 accumulator ``out_acc`` (and ``lse``), one launch per ring step;
+    ``out_final`` (bf16) also receives the result."""
+    lib = _lib.load()
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[3])
+    ds = [_desc(x) for x in (q, k, v, out_acc, lse, out_final)]
+    rc = lib.bea_ring_attention_fwd(*[_ref(x) for x in ds], int(n_chunks), float(softmax_scale),
+                                    int(bool(is_causal)), int(window_size[0]), int(window_size[1]), _stream())
+    _lib.check(rc, "ring_attention_fwd")
+    _count()
+    return out_acc, lse
+
+
+def ring_bwd_workspace_bytes(q, n_chunks) -> int:
+    n, l, h, d = q.shape
+    return int(_lib.load().bea_ring_attention_bwd_workspace_size(n, l, h, d, int(n_chunks)))
+
+
+def ring_attention_bwd_steps(dout, q, k, v, out, lse, dq, dk, dv, n_chunks, softmax_scale=None, is_causal=False,
+                            window_size=(-1, -1), workspace=None):
+    """The whole ring backward replay in one library call: fp32 dq, dk, dv written."""
+    lib = _lib.load()
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[3])
+    if workspace is None:
+        workspace = torch.empty(max(ring_bwd_workspace_bytes(q, n_chunks), 256), dtype=torch.uint8, device=q.device)
+    ds = [_desc(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    rc = lib.bea_ring_attention_bwd(*[_ref(x) for x in ds], int(n_chunks), float(softmax_scale),
+                                    int(bool(is_causal)), int(window_size[0]), int(window_size[1]),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream())
+    _lib.check(rc, "ring_attention_bwd")
+    _count()
+    return dq, dk, dv
+
+
 def device_status() -> int:
     """Synchronise, read and clear the device status word (0 = ok)."""
     return _lib.load().bea_get_device_status(_stream())

@@ -120,13 +120,16 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
     q-dtype output into the fp32 merge). ``fused`` (default: on for bf16
     inputs when no block dtype is asked for) folds each block into the
     accumulator inside the forward kernel instead of writing it out and
-    running ring_merge.
+    running ring_merge; the library then drives every ring step in one call
+    (bea_ring_attention_fwd): one launch per ring step, consecutive launches
+    chained by programmatic dependent launch. The unfused form composes the
+    forward and ring_merge calls here, a pair of launches per ring step.
 
     Every query chunk steps through its K/V chunks in ring order. On one GPU
     the query chunks are independent, so all chunk pairs of one ring step run
     as one call over a batch of chunk views (ring step t pairs query chunk i
-    with K/V chunk i - t): n_chunks launches (plus merges) instead of one per
-    chunk pair. Batches larger than 1 run their rows one after another.
+    with K/V chunk i - t). Batches larger than 1 run their rows one after
+    another.
     ``window_size`` (fused steps only) masks every chunk pair by sequence
     position, with its key chunk placed at its distance from the query chunk;
     pairs entirely outside the window are skipped.
@@ -149,6 +152,11 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
     acc = out if out_dtype == torch.float32 else torch.empty(q.shape, dtype=torch.float32, device=dev)
     c = l // n_chunks
     cast = out_dtype != torch.float32
+    if fused:
+        # the library drives every ring step itself: one launch per step, chained on the stream
+        ops.ring_attention_fwd_steps(q, k, v, acc, lse, n_chunks, softmax_scale, is_causal, window_size,
+                                     out_final=out if cast else None)
+        return out, lse
     for b in range(n):
         qb, kb, vb = q[b:b + 1], k[b:b + 1], v[b:b + 1]
         accb, outb, lseb = acc[b:b + 1], out[b:b + 1], lse[b:b + 1]
@@ -163,9 +171,6 @@ def ring_attention_fwd(q, k, v, n_chunks: int, softmax_scale=None, is_causal=Tru
                     # gets its final output at once
                     ops.flash_mha_fwd(qv, kv_, vv, softmax_scale, is_causal, window_size,
                                       out=fin if fin is not None else av, lse=lv)
-                elif fused:
-                    ops.flash_mha_fwd_merge(qv, kv_, vv, av, lv, softmax_scale, is_causal, window_size,
-                                            out_final=fin, key_offset=koff)
                 else:
                     causal = False  # no window: a live off-diagonal pair sees all its keys
                     blk = torch.empty((cnt, c, h, d), dtype=block_dtype, device=dev)
@@ -181,7 +186,9 @@ def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=Non
 
     ``window_size`` masks each chunk pair by sequence position (key chunk
     placed at its distance from the query chunk, bf16 inputs only); pairs
-    with no visible key are skipped.
+    with no visible key are skipped. bf16 inputs run in one library call
+    (bea_ring_attention_bwd: all chunk pairs of a ring step in one launch);
+    fp32 inputs compose one backward call per chunk pair here.
     """
     n, l, h, d = q.shape
     if softmax_scale is None:
@@ -191,6 +198,11 @@ def ring_attention_bwd(dout, q, k, v, out, lse, n_chunks: int, softmax_scale=Non
     dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
     dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
     dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    if q.dtype == torch.bfloat16:
+        # the library drives every ring step itself: one preprocess, one launch per ring
+        # step (all its chunk pairs), one dQ conversion
+        return ops.ring_attention_bwd_steps(dout, q, k, v, out, lse, dq, dk, dv, n_chunks, softmax_scale, is_causal,
+                                            window_size)
     if not is_causal:
         dq.zero_()
         dk.zero_()

@@ -211,6 +211,61 @@ int bea_flash_mha_bwd_finish(const bea_tensor* dq, float softmax_scale, int accu
                              size_t workspace_bytes, void* stream);
 
 /*
+ * Ring attention replayed on one GPU in one call (flash_attn_jax
+ * flash_sharding.py, "Ring Forward"): the sequence is split into n_chunks
+ * equal chunks; at ring step t query chunk i meets the K/V chunk
+ * (i - t) mod n_chunks (the chunk that started on device i - t when K/V move
+ * i -> i+1), and every live pair's (out, lse) is folded into the running
+ * fp32 (out_acc, lse) by the log-sum-exp merge of bea_flash_mha_fwd_merge.
+ * Pairs whose keys are all masked (under is_causal every pair above the
+ * diagonal; under a window every pair beyond it) are skipped; the window
+ * compares sequence positions, so a chunk pair sees exactly the keys the
+ * single call would. All pairs of one ring step run as one launch over chunk
+ * views; the launches of one call are chained on `stream` by programmatic
+ * dependent launch (a step starts computing while the step before finishes
+ * and merges only after it has).
+ *
+ *   q          [n, l, h, d] bf16; k, v [n, l, h_kv, d] bf16 (same l)
+ *   out_acc    [n, l, h, d] f32, written: the result (the ring's accumulator)
+ *   lse        [n, h, l] f32, written
+ *   out_final  NULL, or [n, l, h, d] bf16: also receives the result cast to
+ *              bf16, written at each query chunk's last live step
+ *   n_chunks   >= 1, dividing l
+ * Errors as for bea_flash_mha_fwd; l % n_chunks != 0 is BEA_ERR_ARG, f32
+ * inputs BEA_ERR_UNSUPPORTED.
+ */
+int bea_ring_attention_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,
+                           const bea_tensor* lse, const bea_tensor* out_final, int n_chunks, float softmax_scale,
+                           int is_causal, int window_left, int window_right, void* stream);
+
+/*
+ * Workspace bytes of bea_ring_attention_bwd for q [n, l, h, d] split into
+ * n_chunks chunks (0 when n_chunks does not divide l).
+ */
+size_t bea_ring_attention_bwd_workspace_size(int64_t n, int64_t l, int64_t h, int64_t d, int n_chunks);
+
+/*
+ * Backward of ring attention on one GPU in one call (flash_attn_jax
+ * flash_sharding.py, "Ring Backward"; picotron context_parallel.py,
+ * RingAttentionFunc.backward): every live chunk pair (same schedule and masks
+ * as bea_ring_attention_fwd) is differentiated once with the FINAL out/lse of
+ * its query rows, and the partial gradients are summed in fp32: dQ of a query
+ * chunk in the workspace accumulator, dK/dV of a key chunk in place. All
+ * pairs of one ring step run as one launch; per batch row: one preprocess,
+ * one launch per live step, one dQ conversion.
+ *
+ *   dout, q    [n, l, h, d] bf16; k, v [n, l, h_kv, d] bf16
+ *   out        [n, l, h, d] bf16 or f32; lse [n, h, l] f32
+ *   dq         [n, l, h, d] f32, written; dk, dv [n, l, h_kv, d] f32, written
+ *   workspace  >= bea_ring_attention_bwd_workspace_size() bytes, 256-byte
+ *              aligned, caller-owned, contents on entry irrelevant
+ */
+int bea_ring_attention_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_tensor* k, const bea_tensor* v,
+                           const bea_tensor* out, const bea_tensor* lse, const bea_tensor* dq, const bea_tensor* dk,
+                           const bea_tensor* dv, int n_chunks, float softmax_scale, int is_causal, int window_left,
+                           int window_right, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * bea_flash_mha_bwd without a caller-supplied workspace. (The pages have no
  * counterpart; this is a library convenience.)
  *

@@ -245,3 +245,37 @@ def test_workspace_size_saturates(lib):
     args = _bwd_args()
     args[1] = T([huge, huge, huge, 128], BF16, strides=[16, 16, 16, 1])
     assert noalloc(lib, args) != OK
+
+
+def test_ring_calls_reject_bad_arguments(lib):
+    r = ctypes.byref
+    q, k, v, o, l = good(l=256)
+    acc = T([1, 256, 4, 128], F32)
+
+    def rf(q_=q, acc_=acc, fin=None, C=2, causal=1, wl=-1, wr=-1, lse=l):
+        return lib.bea_ring_attention_fwd(r(q_), r(k), r(v), r(acc_), r(lse), r(fin) if fin else None, C, 0.1,
+                                          causal, wl, wr, None)
+    assert rf(C=3) == ARG                      # 256 rows do not split into 3 chunks
+    assert rf(C=0) == ARG
+    assert rf(acc_=T([1, 256, 4, 128], BF16)) == DTYPE
+    assert rf(fin=T([1, 256, 4, 128], F32)) == DTYPE
+    assert rf(causal=1, wr=5) == ARG
+    qf, kf, vf, _, _ = good(l=256, dt=F32)
+    assert lib.bea_ring_attention_fwd(r(qf), r(kf), r(vf), r(acc), r(l), None, 2, 0.1, 1, -1, -1, None) == UNSUP
+    q2, k2, v2, _, _ = good(l=256, lk=128)   # ring chunks pair equal lengths only
+    assert lib.bea_ring_attention_fwd(r(q2), r(k2), r(v2), r(acc), r(l), None, 2, 0.1, 0, -1, -1, None) == SHAPE
+    # backward
+    assert lib.bea_ring_attention_bwd_workspace_size(1, 256, 4, 128, 3) == 0
+    ws_need = lib.bea_ring_attention_bwd_workspace_size(1, 16384, 16, 128, 8)
+    assert ws_need == lib.bea_flash_mha_bwd_workspace_size(8, 2048, 16, 128)
+    args = _bwd_args(l=256)
+    ws = FAKE
+
+    def rb(a=args, C=2, nbytes=1 << 30, wsp=ws):
+        return lib.bea_ring_attention_bwd(*[r(x) for x in a], C, 0.1, 1, -1, -1, wsp, nbytes, None)
+    assert rb(C=3) == ARG
+    assert rb(nbytes=16) == WS
+    assert rb(wsp=FAKE + 16) == WS            # not 256-byte aligned
+    bad = list(args)
+    bad[6] = T([1, 256, 4, 128], BF16)        # dq must be f32
+    assert rb(a=bad) == DTYPE

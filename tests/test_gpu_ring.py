@@ -40,7 +40,13 @@ def test_ring_small(causal):
                                         block_dtype=torch.float32)
     so32, sl32 = bea.flash_mha_fwd(q, k, v, scale, causal, out_dtype=torch.float32)
     rob, rlb = bea.ring_attention_fwd(q, k, v, 4, scale, causal)
+    # the library's ring call: the bf16 result is exactly the cast of its fp32 accumulator
+    acc = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lacc = torch.empty((1, 4, 1024), dtype=torch.float32, device="cuda")
+    fin = torch.empty_like(q)
+    bea.ring_attention_fwd_steps(q, k, v, acc, lacc, 4, scale, causal, out_final=fin)
     torch.cuda.synchronize()
+    assert torch.equal(fin, acc.to(torch.bfloat16)) and torch.equal(fin, rob) and torch.equal(lacc, rlb)
     assert_close(to_np(ro32), to_np(so32), TOL_RING, "ring vs single out")
     assert_close(to_np(rl32), to_np(sl32), TOL_RING, "ring vs single lse")
     oo, ol = oracle.ring_fwd_replay(x["q"], x["k"], x["v"], scale, 4, causal)
@@ -96,9 +102,9 @@ def test_ring_full_size():
     # bf16 tolerance against the single call
     bea.launches_since_reset(reset=True)
     rob, rlb = bea.ring_attention_fwd(q, k, v, w.ring_chunks, s, True)
-    # fused, cast to bf16 at each query chunk's last step: per causal step, the chunk that ends
-    # there and the rest (2 * 8 - 1 launches, no merge launches)
-    assert bea.launches_since_reset(reset=True) == 15
+    # fused, one library call: one launch per causal ring step, the bf16 cast of the chunk that
+    # ends at a step written by that step's launch (no merge launches)
+    assert bea.launches_since_reset(reset=True) == 8
     sob, _ = bea.flash_mha_fwd(q, k, v, s, True)
     torch.cuda.synchronize()
     assert float(np.abs(to_np(rob) - to_np(sob)).max()) <= 2e-2
