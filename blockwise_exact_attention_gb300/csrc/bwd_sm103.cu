@@ -633,11 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---- dK / dV epilogue: key warpgroup 0 writes dV, warpgroup 1 writes dK ----
-    // Through shared memory, as the forward's epilogue: each key thread writes 32 fp32 values
-    // of its row (128 bytes, 16-byte pieces of row j rotated by j & 7) into a staging chunk,
-    // then the warpgroup's 128 threads move the chunk as 16-byte pieces, 8 threads per row
-    // segment, so that the accumulate read-modify-write and the stores cover whole 128-byte
-    // segments. The staging buffers are the Q (dV) and dO (dK) stages, free once dkv_full says
+    // Through shared memory, as the forward's epilogue: each key thread writes 128 bytes of its
+    // row (32 fp32 values, or 64 values converted to bf16; 16-byte pieces of row j rotated by
+    // j & 7) into a staging chunk, then the warpgroup's 128 threads move the chunk as 16-byte
+    // pieces, 8 threads per row segment, so that the accumulate read-modify-write and the
+    // stores cover whole 128-byte segments. The staging buffers are the Q (dV) and dO (dK) stages, free once dkv_full says
     // every MMA has completed (never loaded when the CTA saw no query tile).
     if (ok && sc.n_iter > 0) ok = warp_wait_parity(dkv_full, 0, abort_flag, p.status);
     // a dependent launch (the next ring step) adds into dK / dV only after the launch before it is done
@@ -652,27 +652,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t src_t = tmem + lane_base + (c ? T_DK : T_DV);
       const int piece = j & 7;
       const uint32_t ep_id = kEpiBar + c;
+      if (f32) {
+        // fp32 gradients (written, or added to with accumulate): 32 columns per pass
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        if (ok) {
-          uint32_t src[32];
-          if (have) {
-            tmem_ld32(src_t + c0, src);
-            tmem_wait_ld();
-            reg_fence<32>(src);
-          } else {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          if (ok) {
+            uint32_t src[32];
+            if (have) {
+              tmem_ld32(src_t + c0, src);
+              tmem_wait_ld();
+              reg_fence<32>(src);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) src[e] = 0u;
+              for (int e = 0; e < 32; ++e) src[e] = 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(stage + j * 128 + ((k ^ (j & 7)) * 16)) =
+                  make_float4(__uint_as_float(src[4 * k]) * mul, __uint_as_float(src[4 * k + 1]) * mul,
+                              __uint_as_float(src[4 * k + 2]) * mul, __uint_as_float(src[4 * k + 3]) * mul);
           }
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4*>(stage + j * 128 + ((k ^ (j & 7)) * 16)) =
-                make_float4(__uint_as_float(src[4 * k]) * mul, __uint_as_float(src[4 * k + 1]) * mul,
-                            __uint_as_float(src[4 * k + 2]) * mul, __uint_as_float(src[4 * k + 3]) * mul);
-        }
-        named_bar_sync(ep_id, 128);
-        if (ok) {
-          if (f32) {
+          named_bar_sync(ep_id, 128);
+          if (ok) {
             // L2-only loads (.cg): a previous ring step may have written these rows from another SM
             float4 old4[8];
             if (p.accumulate) {
@@ -701,22 +702,52 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst.ptr) + b * dst.sn + (int64_t)key * dst.sl +
                                          kvh * dst.sh + c0 + 4 * piece) = v4;
             }
-          } else {
+          }
+          named_bar_sync(ep_id, 128);
+        }
+      } else {
+        // bf16 gradients: the row threads convert, 64 columns (128 bytes) per pass
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          if (ok) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t src[32];
+              if (have) {
+                tmem_ld32(src_t + c0 + 32 * hf, src);
+                tmem_wait_ld();
+                reg_fence<32>(src);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) src[e] = 0u;
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int e = 8 * k;
+                uint4 v4;
+                v4.x = pack_bf16x2(__uint_as_float(src[e]) * mul, __uint_as_float(src[e + 1]) * mul);
+                v4.y = pack_bf16x2(__uint_as_float(src[e + 2]) * mul, __uint_as_float(src[e + 3]) * mul);
+                v4.z = pack_bf16x2(__uint_as_float(src[e + 4]) * mul, __uint_as_float(src[e + 5]) * mul);
+                v4.w = pack_bf16x2(__uint_as_float(src[e + 6]) * mul, __uint_as_float(src[e + 7]) * mul);
+                const int kk = 4 * hf + k;
+                *reinterpret_cast<uint4*>(stage + j * 128 + ((kk ^ (j & 7)) * 16)) = v4;
+              }
+            }
+          }
+          named_bar_sync(ep_id, 128);
+          if (ok) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const int row = (j >> 3) + 16 * k;
               const int key = sc.k0 + row;
               if (key >= a.lk) continue;
-              const float4 v4 = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
-              uint2 v2;
-              v2.x = pack_bf16x2(v4.x, v4.y);
-              v2.y = pack_bf16x2(v4.z, v4.w);
-              *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dst.ptr) + b * dst.sn +
-                                        (int64_t)key * dst.sl + kvh * dst.sh + c0 + 4 * piece) = v2;
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst.ptr) + b * dst.sn +
+                                        (int64_t)key * dst.sl + kvh * dst.sh + c0 + 8 * piece) =
+                  *reinterpret_cast<const uint4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
             }
           }
+          named_bar_sync(ep_id, 128);
         }
-        named_bar_sync(ep_id, 128);
       }
     }
   } else {
