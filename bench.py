@@ -519,6 +519,20 @@ def main():
         qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True, block_dtype=torch.bfloat16, fused=False), 5, 2))
     rf, rb = attention_flops(1, wr.h, wr.l, wr.l, wr.d, True)
     single_ms = statistics.median(timed(lambda: bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True), 5, 2))
+
+    # host time to issue one ring replay (the calls return before the GPU is done): the library
+    # call issuing all 8 steps, against the same replay composed from Python (forward + merge calls)
+    def host_us(fn, n=20):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        return (t1 - t0) / n * 1e6
+    ring_host_us = host_us(lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True))
+    unfused_host_us = host_us(lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True,
+                                                             block_dtype=torch.bfloat16, fused=False))
     # the ring backward: every live chunk pair once, from the single call's out/lse
     dor = torch.randn_like(qr)
     o_r, l_r = bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True)
@@ -609,10 +623,12 @@ def main():
                   "bound": "hbm", "traffic": ncu_traffic("ring_merge_kernel"),
                   "source_hash": kernel_source_hash("ring_merge_kernel")},
         "ring": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks: the 36 chunk pairs in ring order, one "
-                             "batched call per ring step, 28 pairs as fused ring steps (merge in the forward "
-                             "epilogue); 15 launches", "ms": ring_ms,
+                             "launch per ring step issued by one library call, 28 pairs as fused ring steps "
+                             "(merge in the forward epilogue), steps chained by programmatic dependent launch; "
+                             "8 launches", "ms": ring_ms,
                  "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms,
-                 "unfused_ms": ring_unfused_ms, "unfused": "forward + ring_merge per ring step (bf16 blocks): 15 launches"},
+                 "unfused_ms": ring_unfused_ms, "unfused": "forward + ring_merge per ring step (bf16 blocks): 15 launches",
+                 "host_us_per_call": ring_host_us, "unfused_host_us_per_call": unfused_host_us},
         "ring_bwd": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks: the backward of every live chunk pair "
                                  "(36) once, fp32 dq/dk/dv accumulated over the pairs, from the final out/lse",
                      "ms": ring_bwd_ms, "tflops": rb / (ring_bwd_ms * 1e-3) / 1e12, "launches": ring_bwd_launches,

@@ -101,7 +101,7 @@ struct BwdCfg {
   static constexpr int kDSBytes = 128 * 128 * 2;
   static constexpr int kRowOff = kDSOff + kDSBytes;         // 2 stages of L2[128], D[128] fp32
   static constexpr int kBarOff = kRowOff + 2 * 1024;
-  static constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 2 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot, abort*/;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);    // S_h^T, dP_h^T
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, false, true);     // dV (TMEM A), dK
@@ -321,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;        // Q_i, L2_i, D_i of a stage
+  uint64_t* k_full = bars;            // K and V of the CTA's key block land separately: S needs
+  uint64_t* v_full = bars + 1;        // only K and Q, dP only V and dO
+  uint64_t* q_full = bars + 2;        // Q_i, L2_i, D_i of a stage
   uint64_t* do_full = q_full + 2;
   uint64_t* qdo_empty = do_full + 2;
   uint64_t* sp_full = qdo_empty + 2;  // [2]: S_h^T and dP_h^T of half h are in TMEM slot h
@@ -380,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(kv_full, 1);
+    mbar_init(k_full, 1);
+    mbar_init(v_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&do_full[s], 1);
@@ -415,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-      for (int x = 0; x < C::kBoxes; ++x) {
-        tma_load_4d(smem + C::kKOff + x * 16384, &tk, kv_full, x * 64, kvh, sc.k0, b);
-        tma_load_4d(smem + C::kVOff + x * 16384, &tv, kv_full, x * 64, kvh, sc.k0, b);
-      }
+      // Load order K, Q_0, V, dO_0: the first S products need only K and Q_0 and run while V
+      // and dO_0 arrive.
+      mbar_arrive_expect_tx(k_full, C::kTileBytes);
+      for (int x = 0; x < C::kBoxes; ++x)
+        tma_load_4d(smem + C::kKOff + x * 16384, &tk, k_full, x * 64, kvh, sc.k0, b);
       // With accumulate, the epilogue reads this CTA's dK and dV rows before adding to them.
       // Have L2 fetch them a few rows per iteration, spread over the main loop, so that the
       // epilogues of a wave's CTAs (which end together) do not all read HBM at once.
@@ -447,13 +449,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t row0 = (size_t)(b * a.h + hq) * p.lq_pad + q0;
         bulk_load(smem + C::kRowOff + s * 1024, p.lse2 + row0, kBM * 4, &q_full[s]);
         bulk_load(smem + C::kRowOff + s * 1024 + 512, p.d_row + row0, kBM * 4, &q_full[s]);
+        if (it == 0) {
+          mbar_arrive_expect_tx(v_full, C::kTileBytes);
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(smem + C::kVOff + x * 16384, &tv, v_full, x * 64, kvh, sc.k0, b);
+        }
         mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d(smem + C::kDOOff + s * C::kTileBytes + x * 16384, &tdo, &do_full[s], x * 64, hq, q0, b);
       }
       // loads still in flight must land before shared memory goes away
       volatile int no_abort = 0;
-      wait_parity(kv_full, 0, &no_abort, p.status, 200000000ull);
+      wait_parity(k_full, 0, &no_abort, p.status, 200000000ull);
+      if (it > 0) wait_parity(v_full, 0, &no_abort, p.status, 200000000ull);  // V went out in the first pass
       for (int k = max(0, it - 2); k < it; ++k) {
         wait_parity(&q_full[k & 1], (k >> 1) & 1, &no_abort, p.status, 200000000ull);
         wait_parity(&do_full[k & 1], (k >> 1) & 1, &no_abort, p.status, 200000000ull);
@@ -532,12 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dP_h of the next tile waits for that read.
       // Slot 0 is free for tile i+1 once dV, dK (i) are issued and its dQ_0^T drained, so the
       // key warps' work on each half hides behind the tensor work of the other half.
-      bool ok = sc.n_iter > 0 && warp_wait_parity(kv_full, 0, abort_flag, p.status);
+      bool ok = sc.n_iter > 0 && warp_wait_parity(k_full, 0, abort_flag, p.status);
       if (ok) ok = warp_wait_parity(&q_full[0], 0, abort_flag, p.status);
-      if (ok) ok = warp_wait_parity(&do_full[0], 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
+      }
+      if (ok) ok = warp_wait_parity(v_full, 0, abort_flag, p.status);
+      if (ok) ok = warp_wait_parity(&do_full[0], 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
         issue_dp(0, 0);
         umma_commit_warp(&sp_full[0]);
         issue_s(1, 0);
