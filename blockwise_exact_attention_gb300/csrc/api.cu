@@ -188,27 +188,33 @@ int check_lse(const bea_tensor* lse, const AttnDims& a) {
   return BEA_OK;
 }
 
-// [n, l, h, d] bf16 tensor -> TMA descriptor with 64-column (128-byte) boxes
-// of 128 rows, 128-byte swizzled (the layout the MMA descriptors expect).
-int make_seq_map(const bea_tensor* t, CUtensorMap* map) {
+// [n, l, h, d] tensor -> TMA descriptor with boxes of 128 rows x 128 bytes
+// (box_cols elements of es bytes), 128-byte swizzled.
+static int make_map4(const bea_tensor* t, CUtensorMapDataType dt, int64_t es, cuuint32_t box_cols,
+                     CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   int rc = get_encoder(&enc);
   if (rc) return rc;
   const int64_t d = t->shape[3], hh = t->shape[2], l = t->shape[1], n = t->shape[0];
-  const int64_t es = 2;
   // A size-1 dimension never moves the address; give it a harmless stride.
   const cuuint64_t s_h = (hh > 1) ? t->stride[2] * es : d * es;
   const cuuint64_t s_l = (l > 1) ? t->stride[1] * es : s_h * hh;
   const cuuint64_t s_n = (n > 1) ? t->stride[0] * es : s_l * l;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)hh, (cuuint64_t)l, (cuuint64_t)n};
   cuuint64_t strides[3] = {s_h, s_l, s_n};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {box_cols, 1, 128, 1};
   cuuint32_t es1[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es1,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, dt, 4, t->data, dims, strides, box, es1, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BEA_OK : BEA_ERR_CUDA;
 }
+
+// bf16 [n, l, h, d]: 64-column boxes (the layout the MMA descriptors expect; also the fused
+// ring step's bf16 final copy)
+int make_seq_map(const bea_tensor* t, CUtensorMap* map) { return make_map4(t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, map); }
+
+// fp32 [n, l, h, d] (the fused ring step's accumulator): 32-column boxes
+int make_acc_map(const bea_tensor* t, CUtensorMap* map) { return make_map4(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, map); }
 
 int finish(cudaError_t e, int launches) {
   if (e != cudaSuccess) return BEA_ERR_CUDA;
@@ -392,7 +398,7 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
   if (a.lk > 0) {
     if ((rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv))) return rc;
   }
-  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, s, &launches), launches);
+  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, nullptr, nullptr, s, &launches), launches);
 }
 
 int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,
@@ -432,7 +438,13 @@ int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_
   if (a.lk > 0) {
     if ((rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv))) return rc;
   }
-  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream), &launches), launches);
+  CUtensorMap tacc, tfin;
+  std::memset(&tfin, 0, sizeof(tfin));
+  if ((rc = make_acc_map(out_acc, &tacc))) return rc;
+  if (out_final && (rc = make_seq_map(out_final, &tfin))) return rc;
+  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, &tacc, out_final ? &tfin : nullptr,
+                                     static_cast<cudaStream_t>(stream), &launches),
+                launches);
 }
 
 size_t bea_flash_mha_bwd_workspace_size(int64_t n, int64_t lq, int64_t h, int64_t d) {

@@ -80,9 +80,12 @@ struct FwdParams {
   uint32_t* status;
   int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at tile inject_abort - 1
 };
-// Tensor maps are built by the caller (api.cu) over q, k, v.
+// Tensor maps are built by the caller (api.cu) over q, k, v; for the fused ring step (merge) also
+// over the fp32 accumulator (tacc, 32-column boxes) and, when fin is set, the bf16 final copy
+// (tfin, 64-column boxes). Both may be null for the plain forward.
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, cudaStream_t s, int* nlaunch);
+                            const CUtensorMap& tv, const CUtensorMap* tacc, const CUtensorMap* tfin, cudaStream_t s,
+                            int* nlaunch);
 
 struct BwdParams {
   AttnDims a;

@@ -31,6 +31,8 @@
 // placed before it in the MMA pipeline.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "common.cuh"
 #include "launch_cache.cuh"
 #include "ptx.cuh"
@@ -83,9 +85,13 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + kSub * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1;
-  static constexpr int kEpiOff = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/;  // per-row merge weights
-  static constexpr int kSmemBytes = kEpiOff + kSub * 3 * kBlockM * 4 + 1024 /*align slack*/;
+  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1 + kSub + 2;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
+  // Fused ring step: subtile t's fp32 accumulator rows (128 x D, as D/32 swizzled 32-column
+  // boxes of 16 KB) are staged in the K stages (t = 0) or the V stages (t = 1) once those are
+  // free; the bf16 final copy in the subtile's Q tile.
+  static constexpr int kAccBytes = 128 * D * 4;
+  static_assert(kStages * kTileBytes >= kAccBytes, "a subtile's accumulator fits the K (V) stages");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
   static constexpr uint32_t kVLbo = 64 * 128 * 2;  // byte distance of 64-column V blocks
@@ -121,7 +127,8 @@ __device__ __forceinline__ bool tile_needs_mask(const AttnDims& a, int qs, int j
 template <int D, bool kMerge>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const FwdParams p, float scale_log2) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tacc,
+                    const __grid_constant__ CUtensorMap tfin, const FwdParams p, float scale_log2) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -134,6 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + C::kStages;
   uint64_t* o_full = s_full + kSub;
   uint64_t* mma_done = o_full + kSub;
+  uint64_t* acc_full = mma_done + 1;  // [t]: fused ring step, subtile t's accumulator staged
+  uint64_t* s_done = acc_full + kSub;  // every S product has completed (the K stages are free)
+  uint64_t* pv_done = s_done + 1;      // every P V product has completed (the V stages are free)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -189,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_full[t], 1);
     }
     mbar_init(mma_done, 1);
+    for (int t = 0; t < kSub; ++t) mbar_init(&acc_full[t], 1);
+    mbar_init(s_done, 1);
+    mbar_init(pv_done, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -201,6 +214,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the next kernel on the stream may start as soon as every CTA of this one is running
   grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
+  // Fused ring step: stage subtile t's accumulator rows in shared memory (lane 0 of the producer
+  // for t = 0, of the V-load warp for t = 1) once the stages they go into are free and the
+  // launch this one depends on (the previous ring step) is done. The first step of a ring
+  // reads no accumulator and only says that the stages are free. Returns whether loads went out.
+  auto stage_acc = [&](int t, uint64_t* free_bar) -> bool {
+    const int qs = sc.q0 + t * kBlockM;
+    if (qs >= a.lq) return false;
+    if (!wait_parity(free_bar, 0, abort_flag, p.status)) return false;
+    grid_dependency_wait();
+    if (p.merge_init) {
+      mbar_arrive(&acc_full[t]);
+      return false;
+    }
+    uint8_t* dst = smem + (t == 0 ? C::kKOff : C::kVOff);
+    mbar_arrive_expect_tx(&acc_full[t], C::kAccBytes);
+    for (int c = 0; c < D / 32; ++c) tma_load_4d(dst + c * 16384, &tacc, &acc_full[t], 32 * c, hq, qs, b);
+    return true;
+  };
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
   if (warp == kProducerWarp) {
@@ -210,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+      }
+      if (kMerge) {
+        prefetch_tmap(&tacc);
+        if (p.fin.ptr != nullptr) prefetch_tmap(&tfin);
       }
       uint32_t qbytes = 0;
       for (int t = 0; t < kSub; ++t)
@@ -259,6 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         volatile int no_abort = 0;
         wait_parity(q_full, 0, &no_abort, p.status, 200000000ull);
       }
+      if constexpr (kMerge) {
+        if (stage_acc(0, s_done)) {
+          volatile int no_abort = 0;
+          wait_parity(&acc_full[0], 0, &no_abort, p.status, 200000000ull);
+        }
+      }
     }
   } else if (warp == kVLoadWarp) {
     // ========================== V loads (own ring, own release) ==========================
@@ -279,6 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = max(0, issued - C::kStages); k < issued; ++k) {
         volatile int no_abort = 0;
         wait_parity(&v_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, p.status, 200000000ull);
+      }
+      if constexpr (kMerge) {
+        if (stage_acc(1, pv_done)) {
+          volatile int no_abort = 0;
+          wait_parity(&acc_full[1], 0, &no_abort, p.status, 200000000ull);
+        }
       }
     }
   } else if (warp == kMmaWarp) {
@@ -322,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (lo0 == lo_all && hi0 > lo0) BEA_ISSUE_S(0, 0);
           if (lo1 == lo_all && hi1 > lo1) BEA_ISSUE_S(1, 0);
+          if (hi_all - lo_all == 1) umma_commit_warp(s_done);
           umma_commit_warp(&k_empty[0]);  // K of the first tile is read by nothing else
         }
         int it = 0;
@@ -368,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             BEA_ISSUE_S(1, s1);
           }
+          if (j + 2 == hi_all) umma_commit_warp(s_done);  // the last S products are issued
           if (j + 1 < hi_all) umma_commit_warp(&k_empty[s1]);  // every S of tile j+1 is issued
           umma_commit_warp(&v_empty[s]);                       // every P V of tile j is issued
           if (j == hi0 - 1) umma_commit_warp(&o_full[0]);
@@ -376,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #undef BEA_ISSUE_S
 #undef BEA_ISSUE_PV
+      if (hi_all <= lo_all) umma_commit_warp(s_done);  // no S at all
+      umma_commit_warp(pv_done);
       // After an abort, join the P-ready phases of the tiles not reached (a no-op otherwise).
       for (; pv0 < hi0 - lo0; ++pv0) named_bar_sync(kPReadyBar + 0, kPReadyThreads);
       for (; pv1 < hi1 - lo1; ++pv1) named_bar_sync(kPReadyBar + 1, kPReadyThreads);
@@ -503,29 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u = r;
     const int piece = u & 7;
     const bool init = kMerge && p.merge_init != 0;
-    // Fused ring step: this thread's accumulator pieces of 32 columns (L2-only loads, .cg: under
-    // a dependent launch the previous ring step wrote these rows from other SMs, and no L1 line
-    // of an earlier read may stand in for them).
-    float4 acc4[kMerge ? 8 : 1], accn[kMerge ? 8 : 1];
-    auto load_acc = [&](float4* dst4, int cc) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int qrow = qs + (u >> 3) + 16 * k;
-        if (!init && qrow < a.lq)
-          dst4[k] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out.ptr) +
-                                                           b * p.out.sn + (int64_t)qrow * p.out.sl + hq * p.out.sh +
-                                                           cc + 4 * piece));
-      }
-    };
     float la = -INFINITY;
     if constexpr (kMerge) {
       if (qs < a.lq && !init) {
         // Once the launch this one depends on (the previous ring step) is done, this row's
-        // log-sum-exp and this thread's first accumulator pieces are read while the last P V
-        // completes.
+        // accumulator log-sum-exp is read while the last P V completes (L2-only: the previous
+        // step wrote it from another SM).
         grid_dependency_wait();
         if (row_ok) la = __ldcg(lse_p);
-        if (ok) load_acc(acc4, 0);
       }
     }
     if (ok && have_o) ok = warp_wait_parity(&o_full[t], 0, abort_flag, p.status);
@@ -536,7 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
       const float L = (l_sum > 0.f) ? (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f : -INFINITY;
       uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
-      float* rowv = reinterpret_cast<float*>(smem + C::kEpiOff) + t * 3 * kBlockM;  // per row: wa, wb, keep
       const int ep_id = kEpiBar + t;
       if constexpr (kMerge) {
         // Fused ring step: fold this block's (O, L) into the fp32 accumulator (out, lse) by the
@@ -557,65 +592,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             wb = expf(L - l_new) * inv;
           }
         }
-        rowv[3 * r] = wa;
-        rowv[3 * r + 1] = wb;
-        rowv[3 * r + 2] = keep ? 1.f : 0.f;
         if (ok && row_ok && !keep) *lse_p = l_new;
         const bool fin_on = p.fin.ptr != nullptr && b >= p.fin_b0 && b < p.fin_b1;
-        // the next 32 columns' pieces are loaded while the current ones are combined
+        // The accumulator rows are staged in shared memory as 32-column boxes, 128-byte
+        // swizzled (16-byte piece k of row r at k ^ (r & 7)), so that each row's thread reads and
+        // writes its own row without bank conflicts. The merged box goes back by a TMA store;
+        // the bf16 copy is assembled in the Q tile (64-column boxes) and stored the same way.
+        uint8_t* acc_s = smem + (t == 0 ? C::kKOff : C::kVOff);
+        uint8_t* fin_s = stage;
+        if (ok) ok = warp_wait_parity(&acc_full[t], 0, abort_flag, p.status);
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          if (ok && c0 + 32 < D) load_acc(accn, c0 + 32);
+        for (int c = 0; c < D / 32; ++c) {
           if (ok) {
             uint32_t orow[32];
             if (have_o) {
-              tmem_ld32(o_tmem + c0, orow);
+              tmem_ld32(o_tmem + 32 * c, orow);
               tmem_wait_ld();
               reg_fence<32>(orow);
             } else {
 #pragma unroll
-              for (int c = 0; c < 32; ++c) orow[c] = 0u;
+              for (int e = 0; e < 32; ++e) orow[e] = 0u;
             }
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4*>(stage + r * 128 + ((k ^ (r & 7)) * 16)) =
-                  make_uint4(orow[4 * k], orow[4 * k + 1], orow[4 * k + 2], orow[4 * k + 3]);
-          }
-          named_bar_sync(ep_id, 128);
-          if (ok) {
+            uint8_t* row_s = acc_s + c * 16384 + r * 128;
+            uint8_t* fin_row = fin_s + (c / 2) * 16384 + r * 128;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const int row = (u >> 3) + 16 * k;
-              const int qrow = qs + row;
-              if (qrow >= a.lq) continue;
-              const float rwa = rowv[3 * row], rwb = rowv[3 * row + 1];
-              const bool rkeep = rowv[3 * row + 2] != 0.f;
-              const float4 o = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
+              float4* pa = reinterpret_cast<float4*>(row_s + ((k ^ (r & 7)) * 16));
+              const float o0 = __uint_as_float(orow[4 * k]), o1 = __uint_as_float(orow[4 * k + 1]);
+              const float o2 = __uint_as_float(orow[4 * k + 2]), o3 = __uint_as_float(orow[4 * k + 3]);
               float4 m;
               if (init) {
-                m = make_float4(o.x * rwb, o.y * rwb, o.z * rwb, o.w * rwb);
-              } else if (rkeep) {
-                m = acc4[k];
+                m = make_float4(o0 * wb, o1 * wb, o2 * wb, o3 * wb);
+                *pa = m;
+              } else if (keep) {
+                m = *pa;
               } else {
-                m = make_float4(fmaf(o.x, rwb, acc4[k].x * rwa), fmaf(o.y, rwb, acc4[k].y * rwa),
-                                fmaf(o.z, rwb, acc4[k].z * rwa), fmaf(o.w, rwb, acc4[k].w * rwa));
+                const float4 av = *pa;
+                m = make_float4(fmaf(o0, wb, av.x * wa), fmaf(o1, wb, av.y * wa), fmaf(o2, wb, av.z * wa),
+                                fmaf(o3, wb, av.w * wa));
+                *pa = m;
               }
-              if (!rkeep)
-                *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out.ptr) + b * p.out.sn +
-                                           (int64_t)qrow * p.out.sl + hq * p.out.sh + c0 + 4 * piece) = m;
               if (fin_on) {
-                uint2 v2;
-                v2.x = pack_bf16x2(m.x, m.y);
-                v2.y = pack_bf16x2(m.z, m.w);
-                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.fin.ptr) + b * p.fin.sn +
-                                          (int64_t)qrow * p.fin.sl + hq * p.fin.sh + c0 + 4 * piece) = v2;
+                // columns 32c + 4k .. +3 of the 64-column bf16 box c / 2: byte (c % 2) * 64 + 8k of the row
+                const int pf = (c % 2) * 4 + k / 2;
+                *reinterpret_cast<uint2*>(fin_row + ((pf ^ (r & 7)) * 16) + (k % 2) * 8) =
+                    make_uint2(pack_bf16x2(m.x, m.y), pack_bf16x2(m.z, m.w));
               }
             }
+            fence_proxy_async_smem();  // these writes are read by the TMA stores below
           }
           named_bar_sync(ep_id, 128);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc4[k] = accn[k];
+          if (ok && r == 0) {
+            tma_store_4d(&tacc, acc_s + c * 16384, 32 * c, hq, qs, b);
+            if (fin_on && (c % 2 == 1)) tma_store_4d(&tfin, fin_s + (c / 2) * 16384, 64 * (c / 2), hq, qs, b);
+            bulk_commit_group();
+          }
         }
+        // the stores read shared memory until they complete; the CTA's exit waits for them
+        if (r == 0) bulk_wait_group_all();
       } else {
         if (ok && row_ok) *lse_p = L;
         if (p.out_is_f32) {
@@ -710,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kMerge>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         cudaStream_t s, int* nlaunch) {
+                         const CUtensorMap& tacc, const CUtensorMap& tfin, cudaStream_t s, int* nlaunch) {
   using C = FwdCfg<D>;
   // Once per device context: allow the kernel's dynamic shared memory and read
   // its register count. The register split above is only sound at exactly
@@ -745,7 +779,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtens
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, fwd_bf16_kernel<D, kMerge>, tq, tk, tv, p, scale_log2);
+  e = cudaLaunchKernelEx(&cfg, fwd_bf16_kernel<D, kMerge>, tq, tk, tv, tacc, tfin, p, scale_log2);
   if (e != cudaSuccess) return e;
   *nlaunch += 1;
   return cudaGetLastError();
@@ -754,11 +788,16 @@ cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtens
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            cudaStream_t s, int* nlaunch) {
-  if (p.a.d == 128) return p.merge ? launch_fwd_d<128, true>(p, tq, tk, tv, s, nlaunch)
-                                   : launch_fwd_d<128, false>(p, tq, tk, tv, s, nlaunch);
-  if (p.a.d == 64) return p.merge ? launch_fwd_d<64, true>(p, tq, tk, tv, s, nlaunch)
-                                  : launch_fwd_d<64, false>(p, tq, tk, tv, s, nlaunch);
+                            const CUtensorMap* tacc, const CUtensorMap* tfin, cudaStream_t s, int* nlaunch) {
+  CUtensorMap none;
+  std::memset(&none, 0, sizeof(none));
+  if (p.merge && (tacc == nullptr || (p.fin.ptr != nullptr && tfin == nullptr))) return cudaErrorInvalidValue;
+  const CUtensorMap& ta = tacc ? *tacc : none;
+  const CUtensorMap& tf = tfin ? *tfin : none;
+  if (p.a.d == 128) return p.merge ? launch_fwd_d<128, true>(p, tq, tk, tv, ta, tf, s, nlaunch)
+                                   : launch_fwd_d<128, false>(p, tq, tk, tv, ta, tf, s, nlaunch);
+  if (p.a.d == 64) return p.merge ? launch_fwd_d<64, true>(p, tq, tk, tv, ta, tf, s, nlaunch)
+                                  : launch_fwd_d<64, false>(p, tq, tk, tv, ta, tf, s, nlaunch);
   return cudaErrorInvalidValue;
 }
 

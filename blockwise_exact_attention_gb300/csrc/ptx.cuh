@@ -150,6 +150,22 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// 4-D tile store from shared memory into global memory, completion tracked by
+// bulk async-groups (bulk_commit_group / bulk_wait_group_all). Elements outside
+// the tensor are not written. The shared-memory writes it reads must be made
+// visible to the async proxy first (fence_proxy_async_smem, then a barrier).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has completed (its global writes included).
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

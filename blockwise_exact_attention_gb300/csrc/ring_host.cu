@@ -166,10 +166,13 @@ int bea_ring_attention_fwd(const bea_tensor* q, const bea_tensor* k, const bea_t
         p.pdl = launches > 0;  // the first launch waits for whatever came before it on the stream
         p.status = status;
         p.inject_abort = take_inject_abort();
-        CUtensorMap tq, tk, tv;
-        if ((rc = make_seq_map(&qv, &tq)) || (rc = make_seq_map(&kv, &tk)) || (rc = make_seq_map(&vv, &tv)))
+        CUtensorMap tq, tk, tv, tacc, tfin;
+        if ((rc = make_seq_map(&qv, &tq)) || (rc = make_seq_map(&kv, &tk)) || (rc = make_seq_map(&vv, &tv)) ||
+            (rc = make_acc_map(&av, &tacc)))
           return rc;
-        const cudaError_t e = bea::launch_fwd_bf16(p, tq, tk, tv, s, &launches);
+        if (p.fin.ptr != nullptr && (rc = make_seq_map(&fv, &tfin))) return rc;
+        const cudaError_t e =
+            bea::launch_fwd_bf16(p, tq, tk, tv, &tacc, p.fin.ptr != nullptr ? &tfin : nullptr, s, &launches);
         if (e != cudaSuccess) return finish(e, launches);
         u = w;
       }
