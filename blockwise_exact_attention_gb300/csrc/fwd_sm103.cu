@@ -85,13 +85,17 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + kSub * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1 + kSub + 2;
+  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1 + kSub;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
   // Fused ring step: subtile t's fp32 accumulator rows (128 x D, as D/32 swizzled 32-column
   // boxes of 16 KB) are staged in the K stages (t = 0) or the V stages (t = 1) once those are
   // free; the bf16 final copy in the subtile's Q tile.
-  static constexpr int kAccBytes = 128 * D * 4;
-  static_assert(kStages * kTileBytes >= kAccBytes, "a subtile's accumulator fits the K (V) stages");
+  static constexpr int kBox = 16384;
+  static constexpr int kAccBoxes = D / 32;
+  static constexpr int kBoxesPerStage = kTileBytes / kBox;
+  static constexpr int kAccStages = kAccBoxes / kBoxesPerStage;  // stages one subtile's accumulator takes
+  static_assert(kAccStages * kBoxesPerStage == kAccBoxes && kAccStages <= kStages,
+                "a subtile's accumulator fills whole K (V) stages");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
   static constexpr uint32_t kVLbo = 64 * 128 * 2;  // byte distance of 64-column V blocks
@@ -142,8 +146,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_full = s_full + kSub;
   uint64_t* mma_done = o_full + kSub;
   uint64_t* acc_full = mma_done + 1;  // [t]: fused ring step, subtile t's accumulator staged
-  uint64_t* s_done = acc_full + kSub;  // every S product has completed (the K stages are free)
-  uint64_t* pv_done = s_done + 1;      // every P V product has completed (the V stages are free)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -200,8 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(mma_done, 1);
     for (int t = 0; t < kSub; ++t) mbar_init(&acc_full[t], 1);
-    mbar_init(s_done, 1);
-    mbar_init(pv_done, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -214,23 +214,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the next kernel on the stream may start as soon as every CTA of this one is running
   grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
-  // Fused ring step: stage subtile t's accumulator rows in shared memory (lane 0 of the producer
-  // for t = 0, of the V-load warp for t = 1) once the stages they go into are free and the
-  // launch this one depends on (the previous ring step) is done. The first step of a ring
-  // reads no accumulator and only says that the stages are free. Returns whether loads went out.
-  auto stage_acc = [&](int t, uint64_t* free_bar) -> bool {
+  // Fused ring step: subtile t's accumulator rows are staged in the K (t = 0) or V (t = 1)
+  // stages, taken in the order their last tiles release them: stage i of the accumulator (boxes
+  // [i, i + 1) x kBoxesPerStage) goes where tile ntiles - kStages + i was (a stage no tile used
+  // when that index is negative). acc_stage gives that stage; stage_acc, run by the lane that
+  // fed the ring after its last load, waits for each release (the ring's next phases) and loads
+  // the boxes, once the launch this one depends on (the previous ring step) is done. The first
+  // step of a ring reads no accumulator and only says, once all of them are free, that the
+  // stages may be written. Returns whether loads went out.
+  const int ntiles = sc.hi_all - sc.lo_all;
+  auto acc_stage = [&](int i) { return ((ntiles - C::kStages + i) % C::kStages + C::kStages) % C::kStages; };
+  auto stage_acc = [&](int t, uint64_t* empty, uint8_t* area) -> bool {
     const int qs = sc.q0 + t * kBlockM;
     if (qs >= a.lq) return false;
-    if (!wait_parity(free_bar, 0, abort_flag, p.status)) return false;
-    grid_dependency_wait();
-    if (p.merge_init) {
-      mbar_arrive(&acc_full[t]);
-      return false;
+    bool loading = false;
+    for (int i = 0; i < C::kAccStages; ++i) {
+      const int x = ntiles - C::kStages + i;  // the tile whose release frees this stage
+      if (x >= 0 && !wait_parity(&empty[x % C::kStages], (x / C::kStages) & 1, abort_flag, p.status)) return loading;
+      if (p.merge_init) continue;
+      if (!loading) {
+        grid_dependency_wait();
+        mbar_arrive_expect_tx(&acc_full[t], C::kAccBoxes * C::kBox);
+        loading = true;
+      }
+      uint8_t* dst = area + acc_stage(i) * C::kTileBytes;
+      for (int u = 0; u < C::kBoxesPerStage; ++u) {
+        const int c = i * C::kBoxesPerStage + u;
+        tma_load_4d(dst + u * C::kBox, &tacc, &acc_full[t], 32 * c, hq, qs, b);
+      }
     }
-    uint8_t* dst = smem + (t == 0 ? C::kKOff : C::kVOff);
-    mbar_arrive_expect_tx(&acc_full[t], C::kAccBytes);
-    for (int c = 0; c < D / 32; ++c) tma_load_4d(dst + c * 16384, &tacc, &acc_full[t], 32 * c, hq, qs, b);
-    return true;
+    if (p.merge_init) {
+      grid_dependency_wait();
+      mbar_arrive(&acc_full[t]);
+    }
+    return loading;
   };
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
@@ -259,13 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint64_t pol = l2_policy_evict_last();
-      // Fused ring step: the accumulator rows this CTA folds into are read only in the
-      // epilogue. Have L2 fetch them a few rows per K tile, spread over the main loop: all at
-      // once at the start would queue ahead of the first tiles' loads, and left to the epilogue
-      // the reads of every CTA of a wave (which all end together) would share HBM at once.
-      const int ntiles = sc.hi_all - sc.lo_all;
-      const bool pf = kMerge && !p.merge_init && ntiles > 0;
-      const int pf_per_tile = pf ? (kSub * kBlockM + ntiles - 1) / ntiles : 0;
       int it = 0;
       for (int j = sc.lo_all; j < sc.hi_all; ++j, ++it) {
         const int s = it % C::kStages;
@@ -276,13 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d_hint(kd + x * 16384, &tk, &k_full[s], x * 64, kvh, j * kBlockN, b, pol);
-        for (int rr = it * pf_per_tile; rr < min((it + 1) * pf_per_tile, kSub * kBlockM); ++rr) {
-          const int qrow = sc.q0 + rr;
-          if (qrow < a.lq)
-            bulk_prefetch_l2(reinterpret_cast<const float*>(p.out.ptr) + b * p.out.sn + (int64_t)qrow * p.out.sl +
-                                 hq * p.out.sh,
-                             D * 4);
-        }
       }
       // Loads still in flight must land before the CTA's shared memory goes away.
       const int issued = it;
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_parity(q_full, 0, &no_abort, p.status, 200000000ull);
       }
       if constexpr (kMerge) {
-        if (stage_acc(0, s_done)) {
+        if (issued == ntiles && stage_acc(0, k_empty, smem + C::kKOff)) {
           volatile int no_abort = 0;
           wait_parity(&acc_full[0], 0, &no_abort, p.status, 200000000ull);
         }
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_parity(&v_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, p.status, 200000000ull);
       }
       if constexpr (kMerge) {
-        if (stage_acc(1, pv_done)) {
+        if (issued == ntiles && stage_acc(1, v_empty, smem + C::kVOff)) {
           volatile int no_abort = 0;
           wait_parity(&acc_full[1], 0, &no_abort, p.status, 200000000ull);
         }
@@ -369,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (lo0 == lo_all && hi0 > lo0) BEA_ISSUE_S(0, 0);
           if (lo1 == lo_all && hi1 > lo1) BEA_ISSUE_S(1, 0);
-          if (hi_all - lo_all == 1) umma_commit_warp(s_done);
           umma_commit_warp(&k_empty[0]);  // K of the first tile is read by nothing else
         }
         int it = 0;
@@ -416,7 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             BEA_ISSUE_S(1, s1);
           }
-          if (j + 2 == hi_all) umma_commit_warp(s_done);  // the last S products are issued
           if (j + 1 < hi_all) umma_commit_warp(&k_empty[s1]);  // every S of tile j+1 is issued
           umma_commit_warp(&v_empty[s]);                       // every P V of tile j is issued
           if (j == hi0 - 1) umma_commit_warp(&o_full[0]);
@@ -425,8 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #undef BEA_ISSUE_S
 #undef BEA_ISSUE_PV
-      if (hi_all <= lo_all) umma_commit_warp(s_done);  // no S at all
-      umma_commit_warp(pv_done);
       // After an abort, join the P-ready phases of the tiles not reached (a no-op otherwise).
       for (; pv0 < hi0 - lo0; ++pv0) named_bar_sync(kPReadyBar + 0, kPReadyThreads);
       for (; pv1 < hi1 - lo1; ++pv1) named_bar_sync(kPReadyBar + 1, kPReadyThreads);
@@ -598,7 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // swizzled (16-byte piece k of row r at k ^ (r & 7)), so that each row's thread reads and
         // writes its own row without bank conflicts. The merged box goes back by a TMA store;
         // the bf16 copy is assembled in the Q tile (64-column boxes) and stored the same way.
-        uint8_t* acc_s = smem + (t == 0 ? C::kKOff : C::kVOff);
+        uint8_t* acc_area = smem + (t == 0 ? C::kKOff : C::kVOff);
+        auto acc_box = [&](int c) {
+          return acc_area + acc_stage(c / C::kBoxesPerStage) * C::kTileBytes + (c % C::kBoxesPerStage) * C::kBox;
+        };
         uint8_t* fin_s = stage;
         if (ok) ok = warp_wait_parity(&acc_full[t], 0, abort_flag, p.status);
 #pragma unroll 1
@@ -613,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 32; ++e) orow[e] = 0u;
             }
-            uint8_t* row_s = acc_s + c * 16384 + r * 128;
+            uint8_t* row_s = acc_box(c) + r * 128;
             uint8_t* fin_row = fin_s + (c / 2) * 16384 + r * 128;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -639,11 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint2(pack_bf16x2(m.x, m.y), pack_bf16x2(m.z, m.w));
               }
             }
-            fence_proxy_async_smem();  // these writes are read by the TMA stores below
+            fence_proxy_async_smem();  // these writes are read by the TMA store below
           }
           named_bar_sync(ep_id, 128);
           if (ok && r == 0) {
-            tma_store_4d(&tacc, acc_s + c * 16384, 32 * c, hq, qs, b);
+            tma_store_4d(&tacc, acc_box(c), 32 * c, hq, qs, b);
             if (fin_on && (c % 2 == 1)) tma_store_4d(&tfin, fin_s + (c / 2) * 16384, 64 * (c / 2), hq, qs, b);
             bulk_commit_group();
           }
