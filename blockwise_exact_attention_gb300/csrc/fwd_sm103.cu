@@ -85,7 +85,7 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + kSub * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1 + kSub;
+  static constexpr int kNumBars = 1 + 4 * kStages + 2 * kSub + 1 + kSub * 2;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 /*tmem slot + abort*/ + 1024 /*align slack*/;
   // Fused ring step: subtile t's fp32 accumulator rows (128 x D, as D/32 swizzled 32-column
   // boxes of 16 KB) are staged in the K stages (t = 0) or the V stages (t = 1) once those are
@@ -94,7 +94,7 @@ struct FwdCfg {
   static constexpr int kAccBoxes = D / 32;
   static constexpr int kBoxesPerStage = kTileBytes / kBox;
   static constexpr int kAccStages = kAccBoxes / kBoxesPerStage;  // stages one subtile's accumulator takes
-  static_assert(kAccStages * kBoxesPerStage == kAccBoxes && kAccStages <= kStages,
+  static_assert(kAccStages * kBoxesPerStage == kAccBoxes && kAccStages <= kStages && kAccStages <= 2,
                 "a subtile's accumulator fills whole K (V) stages");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + C::kStages;
   uint64_t* o_full = s_full + kSub;
   uint64_t* mma_done = o_full + kSub;
-  uint64_t* acc_full = mma_done + 1;  // [t]: fused ring step, subtile t's accumulator staged
+  // fused ring step: [t * kAccStages + i]: stage i of subtile t's accumulator has landed
+  uint64_t* acc_full = mma_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_full[t], 1);
     }
     mbar_init(mma_done, 1);
-    for (int t = 0; t < kSub; ++t) mbar_init(&acc_full[t], 1);
+    for (int i = 0; i < kSub * C::kAccStages; ++i) mbar_init(&acc_full[i], 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -224,30 +225,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stages may be written. Returns whether loads went out.
   const int ntiles = sc.hi_all - sc.lo_all;
   auto acc_stage = [&](int i) { return ((ntiles - C::kStages + i) % C::kStages + C::kStages) % C::kStages; };
-  auto stage_acc = [&](int t, uint64_t* empty, uint8_t* area) -> bool {
+  auto stage_acc = [&](int t, uint64_t* empty, uint8_t* area) -> int {
     const int qs = sc.q0 + t * kBlockM;
-    if (qs >= a.lq) return false;
-    bool loading = false;
+    if (qs >= a.lq) return 0;
+    int loaded = 0;  // stages whose loads went out
     for (int i = 0; i < C::kAccStages; ++i) {
       const int x = ntiles - C::kStages + i;  // the tile whose release frees this stage
-      if (x >= 0 && !wait_parity(&empty[x % C::kStages], (x / C::kStages) & 1, abort_flag, p.status)) return loading;
-      if (p.merge_init) continue;
-      if (!loading) {
-        grid_dependency_wait();
-        mbar_arrive_expect_tx(&acc_full[t], C::kAccBoxes * C::kBox);
-        loading = true;
+      if (x >= 0 && !wait_parity(&empty[x % C::kStages], (x / C::kStages) & 1, abort_flag, p.status)) break;
+      if (i == 0) grid_dependency_wait();
+      uint64_t* bar = &acc_full[t * C::kAccStages + i];
+      if (p.merge_init) {
+        mbar_arrive(bar);
+        continue;
       }
+      mbar_arrive_expect_tx(bar, C::kBoxesPerStage * C::kBox);
       uint8_t* dst = area + acc_stage(i) * C::kTileBytes;
       for (int u = 0; u < C::kBoxesPerStage; ++u) {
         const int c = i * C::kBoxesPerStage + u;
-        tma_load_4d(dst + u * C::kBox, &tacc, &acc_full[t], 32 * c, hq, qs, b);
+        tma_load_4d(dst + u * C::kBox, &tacc, bar, 32 * c, hq, qs, b);
       }
+      ++loaded;
     }
-    if (p.merge_init) {
-      grid_dependency_wait();
-      mbar_arrive(&acc_full[t]);
-    }
-    return loading;
+    return loaded;
   };
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
@@ -298,9 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_parity(q_full, 0, &no_abort, p.status, 200000000ull);
       }
       if constexpr (kMerge) {
-        if (issued == ntiles && stage_acc(0, k_empty, smem + C::kKOff)) {
+        const int loaded = issued == ntiles ? stage_acc(0, k_empty, smem + C::kKOff) : 0;
+        for (int i = 0; i < loaded; ++i) {
           volatile int no_abort = 0;
-          wait_parity(&acc_full[0], 0, &no_abort, p.status, 200000000ull);
+          wait_parity(&acc_full[i], 0, &no_abort, p.status, 200000000ull);
         }
       }
     }
@@ -325,9 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_parity(&v_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, p.status, 200000000ull);
       }
       if constexpr (kMerge) {
-        if (issued == ntiles && stage_acc(1, v_empty, smem + C::kVOff)) {
+        const int loaded = issued == ntiles ? stage_acc(1, v_empty, smem + C::kVOff) : 0;
+        for (int i = 0; i < loaded; ++i) {
           volatile int no_abort = 0;
-          wait_parity(&acc_full[1], 0, &no_abort, p.status, 200000000ull);
+          wait_parity(&acc_full[C::kAccStages + i], 0, &no_abort, p.status, 200000000ull);
         }
       }
     }
@@ -602,26 +603,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           return acc_area + acc_stage(c / C::kBoxesPerStage) * C::kTileBytes + (c % C::kBoxesPerStage) * C::kBox;
         };
         uint8_t* fin_s = stage;
-        if (ok) ok = warp_wait_parity(&acc_full[t], 0, abort_flag, p.status);
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        // O_t leaves TMEM one 32-column chunk ahead of the merge: chunk c + 1 loads while chunk c is
+        // merged (two register buffers; the chunk loop is unrolled so that they stay registers)
+        uint32_t oa[32], ob[32];
+        bool pend = false;
+        if (ok && have_o) {
+          tmem_ld32(o_tmem, oa);
+          pend = true;
+        }
+#pragma unroll
+        for (int c = 0; c < C::kAccBoxes; ++c) {
+          uint32_t* cur = (c & 1) ? ob : oa;
+          uint32_t* nxt = (c & 1) ? oa : ob;
+          if (ok && c % C::kBoxesPerStage == 0)  // this stage of the accumulator has landed
+            ok = warp_wait_parity(&acc_full[t * C::kAccStages + c / C::kBoxesPerStage], 0, abort_flag, p.status);
+          if (pend) {
+            tmem_wait_ld();
+            reg_fence<32>(cur);
+            pend = false;
+          }
           if (ok) {
-            uint32_t orow[32];
             if (have_o) {
-              tmem_ld32(o_tmem + 32 * c, orow);
-              tmem_wait_ld();
-              reg_fence<32>(orow);
+              if (c + 1 < C::kAccBoxes) {
+                tmem_ld32(o_tmem + 32 * (c + 1), nxt);
+                pend = true;
+              }
             } else {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) orow[e] = 0u;
+              for (int e = 0; e < 32; ++e) cur[e] = 0u;
             }
             uint8_t* row_s = acc_box(c) + r * 128;
             uint8_t* fin_row = fin_s + (c / 2) * 16384 + r * 128;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               float4* pa = reinterpret_cast<float4*>(row_s + ((k ^ (r & 7)) * 16));
-              const float o0 = __uint_as_float(orow[4 * k]), o1 = __uint_as_float(orow[4 * k + 1]);
-              const float o2 = __uint_as_float(orow[4 * k + 2]), o3 = __uint_as_float(orow[4 * k + 3]);
+              const float o0 = __uint_as_float(cur[4 * k]), o1 = __uint_as_float(cur[4 * k + 1]);
+              const float o2 = __uint_as_float(cur[4 * k + 2]), o3 = __uint_as_float(cur[4 * k + 3]);
               float4 m;
               if (init) {
                 m = make_float4(o0 * wb, o1 * wb, o2 * wb, o3 * wb);
@@ -650,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
+        if (pend) tmem_wait_ld();  // a load still in flight after an abort
         // the stores read shared memory until they complete; the CTA's exit waits for them
         if (r == 0) bulk_wait_group_all();
       } else {
