@@ -398,7 +398,9 @@ int bea_flash_mha_fwd(const bea_tensor* q, const bea_tensor* k, const bea_tensor
   if (a.lk > 0) {
     if ((rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv))) return rc;
   }
-  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, nullptr, nullptr, s, &launches), launches);
+  CUtensorMap tout;  // a bf16 output leaves through TMA stores
+  if (!p.out_is_f32 && (rc = make_seq_map(out, &tout))) return rc;
+  return finish(bea::launch_fwd_bf16(p, tq, tk, tv, nullptr, p.out_is_f32 ? nullptr : &tout, s, &launches), launches);
 }
 
 int bea_flash_mha_fwd_merge(const bea_tensor* q, const bea_tensor* k, const bea_tensor* v, const bea_tensor* out_acc,

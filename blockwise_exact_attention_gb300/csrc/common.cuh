@@ -82,7 +82,8 @@ struct FwdParams {
 };
 // Tensor maps are built by the caller (api.cu) over q, k, v; for the fused ring step (merge) also
 // over the fp32 accumulator (tacc, 32-column boxes) and, when fin is set, the bf16 final copy
-// (tfin, 64-column boxes). Both may be null for the plain forward.
+// (tfin, 64-column boxes). The plain forward takes no tacc, and tfin over its output when that
+// is bf16.
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap* tacc, const CUtensorMap* tfin, cudaStream_t s,
                             int* nlaunch);

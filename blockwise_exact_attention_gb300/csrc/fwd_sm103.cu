@@ -258,10 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
       }
-      if (kMerge) {
-        prefetch_tmap(&tacc);
-        if (p.fin.ptr != nullptr) prefetch_tmap(&tfin);
-      }
+      if (kMerge) prefetch_tmap(&tacc);
+      if (kMerge ? p.fin.ptr != nullptr : !p.out_is_f32) prefetch_tmap(&tfin);
       uint32_t qbytes = 0;
       for (int t = 0; t < kSub; ++t)
         if (sc.lo[t] < sc.hi[t]) qbytes += C::kTileBytes;
@@ -706,9 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(ep_id, 128);
           }
         } else {
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 64) {
-            if (ok) {
+          // bf16 O_t / l: both (all) 64-column boxes staged in the subtile's Q tile, 128-byte
+          // swizzled, then written by TMA stores (tfin is the output's map here)
+          if (ok) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 64) {
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 uint32_t orow[32];
@@ -729,23 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                   v4.z = pack_bf16x2(__uint_as_float(orow[e + 4]) * inv, __uint_as_float(orow[e + 5]) * inv);
                   v4.w = pack_bf16x2(__uint_as_float(orow[e + 6]) * inv, __uint_as_float(orow[e + 7]) * inv);
                   const int kk = 4 * hf + k;
-                  *reinterpret_cast<uint4*>(stage + r * 128 + ((kk ^ (r & 7)) * 16)) = v4;
+                  *reinterpret_cast<uint4*>(stage + (c0 / 64) * 16384 + r * 128 + ((kk ^ (r & 7)) * 16)) = v4;
                 }
               }
             }
-            named_bar_sync(ep_id, 128);
-            if (ok) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int row = (u >> 3) + 16 * k;
-                const int qrow = qs + row;
-                if (qrow >= a.lq) continue;
-                *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out.ptr) + b * p.out.sn +
-                                          (int64_t)qrow * p.out.sl + hq * p.out.sh + c0 + 8 * piece) =
-                    *reinterpret_cast<const uint4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
-              }
-            }
-            named_bar_sync(ep_id, 128);
+            fence_proxy_async_smem();  // these writes are read by the TMA stores below
+          }
+          named_bar_sync(ep_id, 128);
+          if (ok && r == 0) {
+            for (int c = 0; c < D / 64; ++c) tma_store_4d(&tfin, stage + c * 16384, 64 * c, hq, qs, b);
+            bulk_commit_group();
+            bulk_wait_group_all();
           }
         }
       }
@@ -811,7 +805,9 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUt
                             const CUtensorMap* tacc, const CUtensorMap* tfin, cudaStream_t s, int* nlaunch) {
   CUtensorMap none;
   std::memset(&none, 0, sizeof(none));
-  if (p.merge && (tacc == nullptr || (p.fin.ptr != nullptr && tfin == nullptr))) return cudaErrorInvalidValue;
+  if (p.merge && tacc == nullptr) return cudaErrorInvalidValue;
+  // tfin: the merge's bf16 final copy, or the plain forward's bf16 output
+  if ((p.merge ? p.fin.ptr != nullptr : !p.out_is_f32) && tfin == nullptr) return cudaErrorInvalidValue;
   const CUtensorMap& ta = tacc ? *tacc : none;
   const CUtensorMap& tf = tfin ? *tfin : none;
   if (p.a.d == 128) return p.merge ? launch_fwd_d<128, true>(p, tq, tk, tv, ta, tf, s, nlaunch)
