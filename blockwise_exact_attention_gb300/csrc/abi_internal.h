@@ -37,6 +37,7 @@ int check_lse(const bea_tensor* lse, const AttnDims& a);
 // TMA descriptor over a [n, l, h, d] bf16 tensor: 64-column boxes of 128 rows, 128-byte swizzle.
 int make_seq_map(const bea_tensor* t, CUtensorMap* map);
 int make_acc_map(const bea_tensor* t, CUtensorMap* map);
+int make_grad_map(const bea_tensor* g, CUtensorMap* map);
 
 // Backward workspace: [dq_acc | D | lse2], each region [n, h, lq_pad(, d)] and 256-byte aligned.
 struct BwdWorkspace {

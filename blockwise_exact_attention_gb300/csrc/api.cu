@@ -213,6 +213,11 @@ static int make_map4(const bea_tensor* t, CUtensorMapDataType dt, int64_t es, cu
 // ring step's bf16 final copy)
 int make_seq_map(const bea_tensor* t, CUtensorMap* map) { return make_map4(t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, map); }
 
+// dK / dV of the backward: bf16 64-column or fp32 32-column boxes
+int make_grad_map(const bea_tensor* g, CUtensorMap* map) {
+  return g->dtype == BEA_F32 ? make_acc_map(g, map) : make_seq_map(g, map);
+}
+
 // fp32 [n, l, h, d] (the fused ring step's accumulator): 32-column boxes
 int make_acc_map(const bea_tensor* t, CUtensorMap* map) { return make_map4(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, map); }
 
@@ -493,17 +498,20 @@ int bea_flash_mha_bwd(const bea_tensor* dout, const bea_tensor* q, const bea_ten
   set_workspace(&p, workspace, w);
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
   p.inject_abort = take_inject_abort();
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   std::memset(&tq, 0, sizeof(tq));
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
   std::memset(&tdo, 0, sizeof(tdo));
+  std::memset(&tdk, 0, sizeof(tdk));
+  std::memset(&tdv, 0, sizeof(tdv));
   if (a.lq > 0 && a.lk > 0) {
     if ((rc = make_seq_map(q, &tq)) || (rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv)) ||
         (rc = make_seq_map(dout, &tdo)))
       return rc;
   }
-  return finish(bea::launch_bwd_bf16(p, tq, tk, tv, tdo, s, &launches), launches);
+  if (a.lk > 0 && ((rc = make_grad_map(dk, &tdk)) || (rc = make_grad_map(dv, &tdv)))) return rc;
+  return finish(bea::launch_bwd_bf16(p, tq, tk, tv, tdo, tdk, tdv, s, &launches), launches);
 }
 
 int bea_flash_mha_bwd_prepare(const bea_tensor* dout, const bea_tensor* out, const bea_tensor* lse,
@@ -560,17 +568,21 @@ int bea_flash_mha_bwd_kv_block(const bea_tensor* dout, const bea_tensor* q, cons
   set_workspace(&p, workspace, w);
   if ((rc = status_ptr_for_current_device(&p.status))) return rc;
   p.inject_abort = take_inject_abort();
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   std::memset(&tq, 0, sizeof(tq));
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
   std::memset(&tdo, 0, sizeof(tdo));
+  std::memset(&tdk, 0, sizeof(tdk));
+  std::memset(&tdv, 0, sizeof(tdv));
   if (a.lq > 0 && a.lk > 0) {
     if ((rc = make_seq_map(q, &tq)) || (rc = make_seq_map(k, &tk)) || (rc = make_seq_map(v, &tv)) ||
         (rc = make_seq_map(dout, &tdo)))
       return rc;
   }
-  return finish(bea::launch_bwd_main(p, tq, tk, tv, tdo, static_cast<cudaStream_t>(stream), &launches), launches);
+  if (a.lk > 0 && ((rc = make_grad_map(dk, &tdk)) || (rc = make_grad_map(dv, &tdv)))) return rc;
+  return finish(bea::launch_bwd_main(p, tq, tk, tv, tdo, tdk, tdv, static_cast<cudaStream_t>(stream), &launches),
+                launches);
 }
 
 int bea_flash_mha_bwd_finish(const bea_tensor* dq, float softmax_scale, int accumulate, void* workspace,

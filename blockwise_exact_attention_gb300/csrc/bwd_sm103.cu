@@ -317,6 +317,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                     const BwdParams p, float scale_log2) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -417,31 +418,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
+      prefetch_tmap(&tdk);
+      prefetch_tmap(&tdv);
       // Load order K, Q_0, V, dO_0: the first S products need only K and Q_0 and run while V
       // and dO_0 arrive.
       mbar_arrive_expect_tx(k_full, C::kTileBytes);
       for (int x = 0; x < C::kBoxes; ++x)
         tma_load_4d(smem + C::kKOff + x * 16384, &tk, k_full, x * 64, kvh, sc.k0, b);
-      // With accumulate, the epilogue reads this CTA's dK and dV rows before adding to them.
-      // Have L2 fetch them a few rows per iteration, spread over the main loop, so that the
-      // epilogues of a wave's CTAs (which end together) do not all read HBM at once.
-      const int pf_per_it = p.accumulate ? (kBN + sc.n_iter - 1) / sc.n_iter : 0;
       int it = 0;
       for (; it < sc.n_iter; ++it) {
         const int s = it & 1;
         const int hq = kvh * sc.g + it / nt;
         const int q0 = (sc.i_lo + it % nt) * kBM;
-        for (int rr = it * pf_per_it; rr < min((it + 1) * pf_per_it, kBN); ++rr) {
-          const int key = sc.k0 + rr;
-          if (key < a.lk) {
-            bulk_prefetch_l2(reinterpret_cast<const float*>(p.dk.ptr) + b * p.dk.sn + (int64_t)key * p.dk.sl +
-                                 kvh * p.dk.sh,
-                             D * 4);
-            bulk_prefetch_l2(reinterpret_cast<const float*>(p.dv.ptr) + b * p.dv.sn + (int64_t)key * p.dv.sl +
-                                 kvh * p.dv.sh,
-                             D * 4);
-          }
-        }
         if (it >= 2 && !wait_parity(&qdo_empty[s], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&q_full[s], C::kTileBytes + 2 * kBM * 4);
         for (int x = 0; x < C::kBoxes; ++x)
@@ -645,12 +633,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---- dK / dV epilogue: key warpgroup 0 writes dV, warpgroup 1 writes dK ----
-    // Through shared memory, as the forward's epilogue: each key thread writes 128 bytes of its
-    // row (32 fp32 values, or 64 values converted to bf16; 16-byte pieces of row j rotated by
-    // j & 7) into a staging chunk, then the warpgroup's 128 threads move the chunk as 16-byte
-    // pieces, 8 threads per row segment, so that the accumulate read-modify-write and the
-    // stores cover whole 128-byte segments. The staging buffers are the Q (dV) and dO (dK) stages, free once dkv_full says
-    // every MMA has completed (never loaded when the CTA saw no query tile).
+    // Through shared memory: each key thread writes 128 bytes of its row (32 fp32 values, or 64
+    // converted to bf16; the 16-byte pieces of row j rotated by j & 7) into a staging chunk. With
+    // accumulate, TMA adds the staged rows to dK / dV element by element at L2 (the 128-byte
+    // swizzle of the gradient's tensor map); otherwise the warpgroup's 128 threads store the
+    // chunk as 16-byte pieces, 8 threads per 128-byte row segment. The staging buffers are the Q
+    // (dV) and dO (dK) stages, free once dkv_full says every MMA has completed (never loaded when
+    // the CTA saw no query tile).
     if (ok && sc.n_iter > 0) ok = warp_wait_parity(dkv_full, 0, abort_flag, p.status);
     // a dependent launch (the next ring step) adds into dK / dV only after the launch before it is done
     grid_dependency_wait();
@@ -659,13 +648,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool have = sc.n_iter > 0;
       const float mul = c ? a.scale : 1.f;
       const bool f32 = c ? p.dk_is_f32 : p.dv_is_f32;
+      const CUtensorMap* tmap = c ? &tdk : &tdv;
       const Seq4 dst = c ? p.dk : p.dv;
+      const int piece = j & 7;
       uint8_t* stage = smem + (c ? C::kDOOff : C::kQOff);
       const uint32_t src_t = tmem + lane_base + (c ? T_DK : T_DV);
-      const int piece = j & 7;
       const uint32_t ep_id = kEpiBar + c;
-      if (f32) {
-        // fp32 gradients (written, or added to with accumulate): 32 columns per pass
+      if (f32 && p.accumulate) {
+        // fp32 added to (a ring step after the first): D / 32 boxes of 32 columns staged, then
+        // added element by element at L2 by TMA (no read of the old values here)
+        if (ok) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t src[32];
+            if (have) {
+              tmem_ld32(src_t + c0, src);
+              tmem_wait_ld();
+              reg_fence<32>(src);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) src[e] = 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(stage + (c0 / 32) * 16384 + j * 128 + ((k ^ (j & 7)) * 16)) =
+                  make_float4(__uint_as_float(src[4 * k]) * mul, __uint_as_float(src[4 * k + 1]) * mul,
+                              __uint_as_float(src[4 * k + 2]) * mul, __uint_as_float(src[4 * k + 3]) * mul);
+          }
+          fence_proxy_async_smem();  // these writes are read by the TMA reductions below
+        }
+        named_bar_sync(ep_id, 128);
+        if (ok && j == 0) {
+          // (rows past the last key are not touched)
+          for (int x = 0; x < D / 32; ++x) tma_reduce_add_4d(tmap, stage + x * 16384, 32 * x, kvh, sc.k0, b);
+          bulk_commit_group();
+          // (a launch that depends on this one programmatically also needs the additions done)
+          if (p.pdl_next) bulk_wait_group_all();
+          else bulk_wait_group_read_all();
+        }
+      } else if (f32) {
+        // fp32 gradients written: 32 columns per pass
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           if (ok) {
@@ -686,31 +708,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           named_bar_sync(ep_id, 128);
           if (ok) {
-            // L2-only loads (.cg): a previous ring step may have written these rows from another SM
-            float4 old4[8];
-            if (p.accumulate) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int row = (j >> 3) + 16 * k;
-                const int key = sc.k0 + row;
-                if (key < a.lk)
-                  old4[k] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(dst.ptr) +
-                                                                   b * dst.sn + (int64_t)key * dst.sl +
-                                                                   kvh * dst.sh + c0 + 4 * piece));
-              }
-            }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const int row = (j >> 3) + 16 * k;
               const int key = sc.k0 + row;
               if (key >= a.lk) continue;  // ragged last key block
-              float4 v4 = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
-              if (p.accumulate) {
-                v4.x += old4[k].x;
-                v4.y += old4[k].y;
-                v4.z += old4[k].z;
-                v4.w += old4[k].w;
-              }
+              const float4 v4 = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) * 16));
               *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst.ptr) + b * dst.sn + (int64_t)key * dst.sl +
                                          kvh * dst.sh + c0 + 4 * piece) = v4;
             }
@@ -812,7 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
+                              const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s,
+                              int* nlaunch) {
   using C = BwdCfg<D>;
   const AttnDims& a = p.a;
   const int nkb = (a.lk + kBN - 1) / kBN;
@@ -848,7 +852,7 @@ cudaError_t launch_bwd_main_d(const BwdParams& p, const CUtensorMap& tq, const C
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, bwd_bf16_kernel<D>, tq, tk, tv, tdo, p, scale_log2);
+  e = cudaLaunchKernelEx(&cfg, bwd_bf16_kernel<D>, tq, tk, tv, tdo, tdk, tdv, p, scale_log2);
   if (e != cudaSuccess) return e;
   *nlaunch += 1;
   return cudaGetLastError();
@@ -884,9 +888,10 @@ cudaError_t launch_bwd_prepare(const BwdParams& p, cudaStream_t s, int* nlaunch)
 }
 
 cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
-  if (p.a.d == 128) return launch_bwd_main_d<128>(p, tq, tk, tv, tdo, s, nlaunch);
-  if (p.a.d == 64) return launch_bwd_main_d<64>(p, tq, tk, tv, tdo, s, nlaunch);
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s,
+                            int* nlaunch) {
+  if (p.a.d == 128) return launch_bwd_main_d<128>(p, tq, tk, tv, tdo, tdk, tdv, s, nlaunch);
+  if (p.a.d == 64) return launch_bwd_main_d<64>(p, tq, tk, tv, tdo, tdk, tdv, s, nlaunch);
   return cudaErrorInvalidValue;
 }
 
@@ -906,11 +911,12 @@ cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch) 
 }
 
 cudaError_t launch_bwd_bf16(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, cudaStream_t s, int* nlaunch) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t s,
+                            int* nlaunch) {
   if (p.a.d != 64 && p.a.d != 128) return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = launch_bwd_prepare(p, s, nlaunch)) != cudaSuccess) return e;
-  if ((e = launch_bwd_main(p, tq, tk, tv, tdo, s, nlaunch)) != cudaSuccess) return e;
+  if ((e = launch_bwd_main(p, tq, tk, tv, tdo, tdk, tdv, s, nlaunch)) != cudaSuccess) return e;
   return launch_bwd_finish(p, s, nlaunch);
 }
 

@@ -77,6 +77,7 @@ struct FwdParams {
   Seq4 fin;   // merge only: bf16 copy of the merged rows, ptr may be null
   int fin_b0, fin_b1;  // merge only: fin is written for batch indices [fin_b0, fin_b1) only
   int pdl;    // launch with programmatic stream serialisation (see grid_dependency_wait)
+  int pdl_next;  // the next launch on the stream depends on this one programmatically
   uint32_t* status;
   int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at tile inject_abort - 1
 };
@@ -99,19 +100,23 @@ struct BwdParams {
   float* lse2;    // workspace: [n, h, lq_pad] lse * log2(e), +inf for rows without keys / padding
   int lq_pad;
   int pdl;        // launch with programmatic stream serialisation (see grid_dependency_wait)
+  int pdl_next;   // the next launch on the stream depends on this one programmatically
   uint32_t* status;
   int inject_abort;  // test hook, 0 = off: CTA 0's MMA warp aborts at iteration inject_abort - 1
 };
-// Tensor maps over q, k, v, dout are built by the caller (api.cu).
+// Tensor maps over q, k, v, dout and the gradients dk, dv (make_grad_map: bf16 64-column or fp32
+// 32-column boxes of 128 rows) are built by the caller (api.cu).
 // launch_bwd_bf16 = prepare (D, lse*log2e, zeroed dQ accumulator) + main
 // (dK, dV, dQ accumulation) + finish (dQ = scale * accumulator); the stages
 // are also exported separately for callers that accumulate dQ over several
 // K/V blocks.
 cudaError_t launch_bwd_bf16(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s, int* nlaunch);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, cudaStream_t s, int* nlaunch);
 cudaError_t launch_bwd_prepare(const BwdParams& p, cudaStream_t s, int* nlaunch);
 cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s, int* nlaunch);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, cudaStream_t s, int* nlaunch);
 cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch);
 
 cudaError_t launch_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, cudaStream_t s);

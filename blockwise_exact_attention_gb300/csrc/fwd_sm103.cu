@@ -739,7 +739,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && r == 0) {
             for (int c = 0; c < D / 64; ++c) tma_store_4d(&tfin, stage + c * 16384, 64 * c, hq, qs, b);
             bulk_commit_group();
-            bulk_wait_group_all();
+            // (a launch that depends on this one programmatically also needs the writes done)
+            if (p.pdl_next) bulk_wait_group_all();
+            else bulk_wait_group_read_all();
           }
         }
       }

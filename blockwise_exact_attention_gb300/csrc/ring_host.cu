@@ -164,6 +164,7 @@ int bea_ring_attention_fwd(const bea_tensor* q, const bea_tensor* k, const bea_t
         p.fin_b0 = f0 - u;
         p.fin_b1 = f1 - u;
         p.pdl = launches > 0;  // the first launch waits for whatever came before it on the stream
+        p.pdl_next = 1;
         p.status = status;
         p.inject_abort = take_inject_abort();
         CUtensorMap tq, tk, tv, tacc, tfin;
@@ -249,12 +250,13 @@ int bea_ring_attention_bwd(const bea_tensor* dout, const bea_tensor* q, const be
       p.d_row = base.d_row + (size_t)r.i0 * rows_per_chunk;
       p.lse2 = base.lse2 + (size_t)r.i0 * rows_per_chunk;
       p.pdl = r.t > 0;  // step 0 follows the preprocess, whose results it reads at once
+      p.pdl_next = 1;   // the next step adds into the same dK / dV as soon as this one is done
       p.inject_abort = take_inject_abort();
-      CUtensorMap tq, tk, tv, tdo;
+      CUtensorMap tq, tk, tv, tdo, tdk, tdv;
       if ((rc = make_seq_map(&qv, &tq)) || (rc = make_seq_map(&kv, &tk)) || (rc = make_seq_map(&vv, &tv)) ||
-          (rc = make_seq_map(&dov_r, &tdo)))
+          (rc = make_seq_map(&dov_r, &tdo)) || (rc = make_grad_map(&dkv, &tdk)) || (rc = make_grad_map(&dvv, &tdv)))
         return rc;
-      e = bea::launch_bwd_main(p, tq, tk, tv, tdo, s, &launches);
+      e = bea::launch_bwd_main(p, tq, tk, tv, tdo, tdk, tdv, s, &launches);
       if (e != cudaSuccess) return finish(e, launches);
     }
     // dQ = scale x accumulator for every query row of batch b
