@@ -43,14 +43,20 @@ L2_FLUSH_BYTES = 256 << 20
 # figure no longer describes the kernel, and the JSON line reports null.
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, source hash at capture)
-    "bwd_bf16_kernel<128>": (616.1e6 + 271.9e6, "3959272bec4f"),   # causal GQA 8k, one launch
-    "fwd_bf16_kernel<128>": (101.1e6 + 36.5e6, "5cec3981bd85"),    # causal GQA 8k, one launch
-    "ring_merge_kernel": (204.1e6 + 76.6e6, "ba0f6b58f203"),       # [1,16384,16,128], L2 flushed before
+    "bwd_bf16_kernel<128>": (612.2e6 + 270.9e6, "2c8ece653741"),   # causal GQA 8k, one launch
+    "fwd_bf16_kernel<128>": (101.1e6 + 36.5e6, "e08e3609a164"),    # causal GQA 8k, one launch
+    "ring_merge_kernel": (204.1e6 + 75.9e6, "531d70872b16"),       # [1,16384,16,128], L2 flushed before
+    # the fused ring step of the 16k ring, step 1 (7 chunk pairs, 896 CTAs); same sources as the forward
+    "fwd_bf16_kernel<128, merge>": (294.7e6 + 90.3e6, "e08e3609a164"),
 }
+# Algorithmic bytes of that fused step: q, k, v (bf16) of 7 chunks of [2048, 16, 128], the fp32
+# accumulator read and written, the log-sum-exp read and written.
+RING_STEP1_BYTES = 7 * 2048 * 16 * (3 * 128 * 2 + 2 * 128 * 4 + 2 * 4)
 KERNEL_SOURCES = {
     "bwd_bf16_kernel<128>": ("bwd_sm103.cu", "ptx.cuh", "common.cuh"),
     "fwd_bf16_kernel<128>": ("fwd_sm103.cu", "ptx.cuh", "common.cuh"),
     "ring_merge_kernel": ("merge.cu", "common.cuh"),
+    "fwd_bf16_kernel<128, merge>": ("fwd_sm103.cu", "ptx.cuh", "common.cuh"),
 }
 
 
@@ -628,7 +634,9 @@ def main():
                              "8 launches", "ms": ring_ms,
                  "tflops": rf / (ring_ms * 1e-3) / 1e12, "single_call_ms": single_ms,
                  "unfused_ms": ring_unfused_ms, "unfused": "forward + ring_merge per ring step (bf16 blocks): 15 launches",
-                 "host_us_per_call": ring_host_us, "unfused_host_us_per_call": unfused_host_us},
+                 "host_us_per_call": ring_host_us, "unfused_host_us_per_call": unfused_host_us,
+                 "step1_traffic": ncu_traffic("fwd_bf16_kernel<128, merge>"), "step1_algorithmic_bytes": RING_STEP1_BYTES,
+                 "step1": "ncu DRAM bytes of ring step 1 (7 fused chunk pairs) against its algorithmic bytes"},
         "ring_bwd": {"workload": "causal bf16 [1,16384,16,128] as 8 chunks: the backward of every live chunk pair "
                                  "(36) once, fp32 dq/dk/dv accumulated over the pairs, from the final out/lse",
                      "ms": ring_bwd_ms, "tflops": rb / (ring_bwd_ms * 1e-3) / 1e12, "launches": ring_bwd_launches,
