@@ -286,3 +286,44 @@ def test_ring_call_batches_and_final_cast(causal, window):
         assert_close(to_np(a), to_np(b_), TOL_RING, name + " ring call vs single")
         assert_close_bf16(to_np(a), r, name + " ring call", output_is_bf16=False)
     assert bea.device_status() == 0
+
+
+# ---- chunks that are not a multiple of the 128-row tiles ------------------------------------
+
+@pytest.mark.parametrize("d,causal,window", [(128, True, (-1, -1)), (64, False, (200, 100)), (128, True, (300, 0))])
+def test_ring_ragged_chunks(d, causal, window):
+    """Chunks of 120 rows: each chunk's last 128-row tile runs past its end into the next chunk,
+    so the fused forward's accumulator stores and the ring backward's dK/dV additions must stop
+    at the chunk's end (neighbouring chunks keep their own rows). Forward and backward against the
+    oracle's ring replay and the single call."""
+    import blockwise_exact_attention_gb300 as bea
+    n, C, c, h, hkv = 1, 8, 120, 4, 2
+    l = C * c
+    x = workloads.small_case(n=n, l=l, h=h, h_kv=hkv, d=d, is_causal=causal, window=window, seed=90 + d)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (to_dev(x[s_], torch.bfloat16) for s_ in ("q", "k", "v", "dout"))
+    acc = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty((n, h, l), dtype=torch.float32, device="cuda")
+    fin = torch.empty_like(q)
+    bea.ring_attention_fwd_steps(q, k, v, acc, lse, C, scale, causal, window, out_final=fin)
+    so, sl = bea.flash_mha_fwd(q, k, v, scale, causal, window, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    assert torch.equal(fin, acc.to(torch.bfloat16))
+    a_abs, _ = oracle.attention_fwd(x["q"], x["k"], np.abs(x["v"]), scale, causal, window)
+    assert_within(to_np(acc), to_np(so), ring_out_bound(a_abs), "ragged ring vs single out")
+    assert_close(to_np(lse), to_np(sl), TOL_RING, "ragged ring vs single lse")
+    oo, ol = oracle.ring_fwd_replay(x["q"], x["k"], x["v"], scale, C, causal, window)
+    assert_close_bf16(to_np(acc), oo, "ragged ring out vs oracle", output_is_bf16=False)
+    assert_close(to_np(lse), ol, TOL_LSE, "ragged ring lse vs oracle")
+    o_up = workloads.round_to_bf16(oo.astype(np.float32))
+    l_up = ol.astype(np.float32)
+    o, lt = to_dev(o_up, torch.bfloat16), to_dev(l_up, torch.float32)
+    rg = bea.ring_attention_bwd(do, q, k, v, o, lt, C, scale, causal, window)
+    sg = bea.flash_mha_bwd(do, q, k, v, o, lt, scale, causal, window, grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    ref = oracle.ring_bwd_replay(x["dout"], x["q"], x["k"], x["v"], o_up, l_up, scale, C, causal, window)
+    for name, a, b_, r in zip(("dq", "dk", "dv"), rg, sg, ref):
+        assert_close(to_np(a), to_np(b_), TOL_RING, name + " ragged ring vs single")
+        assert_close_bf16(to_np(a), r, name + " ragged ring", output_is_bf16=False)
