@@ -380,7 +380,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nt = sc.i_hi - sc.i_lo;
 
-  if (threadIdx.x == 0) {
+  // The producer's loads of iteration it: Q_i with its L log2e and D rows, the CTA's V (with the
+  // first), dO_i. Load order K, Q_0, V, dO_0: the first S products need only K and Q_0 and run
+  // while V and dO_0 arrive.
+  auto issue_iter = [&](int it) {
+    const int s = it & 1;
+    const int hq = kvh * sc.g + it / nt;
+    const int q0 = (sc.i_lo + it % nt) * kBM;
+    mbar_arrive_expect_tx(&q_full[s], C::kTileBytes + 2 * kBM * 4);
+    for (int x = 0; x < C::kBoxes; ++x)
+      tma_load_4d(smem + C::kQOff + s * C::kTileBytes + x * 16384, &tq, &q_full[s], x * 64, hq, q0, b);
+    const size_t row0 = (size_t)(b * a.h + hq) * p.lq_pad + q0;
+    bulk_load(smem + C::kRowOff + s * 1024, p.lse2 + row0, kBM * 4, &q_full[s]);
+    bulk_load(smem + C::kRowOff + s * 1024 + 512, p.d_row + row0, kBM * 4, &q_full[s]);
+    if (it == 0) {
+      mbar_arrive_expect_tx(v_full, C::kTileBytes);
+      for (int x = 0; x < C::kBoxes; ++x)
+        tma_load_4d(smem + C::kVOff + x * 16384, &tv, v_full, x * 64, kvh, sc.k0, b);
+    }
+    mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
+    for (int x = 0; x < C::kBoxes; ++x)
+      tma_load_4d(smem + C::kDOOff + s * C::kTileBytes + x * 16384, &tdo, &do_full[s], x * 64, hq, q0, b);
+  };
+
+  // The producer's lane initialises the barriers and sends the loads that wait on nothing (K and
+  // the first two iterations' Q/dO) before the CTA-wide barrier, so that they are in flight while
+  // TMEM is allocated and the other warps arrive.
+  int it_early = 0;  // producer lane: iterations already issued
+  if (threadIdx.x == kProducerWarp * 32) {
     *abort_flag = 0;
     mbar_init(k_full, 1);
     mbar_init(v_full, 1);
@@ -395,6 +422,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dkv_full, 1);
     mbar_init(mma_done, 1);
     fence_mbar_init();
+    if (sc.n_iter > 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      prefetch_tmap(&tdk);
+      prefetch_tmap(&tdv);
+      mbar_arrive_expect_tx(k_full, C::kTileBytes);
+      for (int x = 0; x < C::kBoxes; ++x)
+        tma_load_4d(smem + C::kKOff + x * 16384, &tk, k_full, x * 64, kvh, sc.k0, b);
+      for (; it_early < 2 && it_early < sc.n_iter; ++it_early) issue_iter(it_early);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
@@ -414,37 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ========================== TMA producer ==========================
     if (lane == 0 && sc.n_iter > 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-      prefetch_tmap(&tdo);
-      prefetch_tmap(&tdk);
-      prefetch_tmap(&tdv);
-      // Load order K, Q_0, V, dO_0: the first S products need only K and Q_0 and run while V
-      // and dO_0 arrive.
-      mbar_arrive_expect_tx(k_full, C::kTileBytes);
-      for (int x = 0; x < C::kBoxes; ++x)
-        tma_load_4d(smem + C::kKOff + x * 16384, &tk, k_full, x * 64, kvh, sc.k0, b);
-      int it = 0;
+      // (K and the first two iterations went out during the setup)
+      int it = it_early;
       for (; it < sc.n_iter; ++it) {
-        const int s = it & 1;
-        const int hq = kvh * sc.g + it / nt;
-        const int q0 = (sc.i_lo + it % nt) * kBM;
-        if (it >= 2 && !wait_parity(&qdo_empty[s], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&q_full[s], C::kTileBytes + 2 * kBM * 4);
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d(smem + C::kQOff + s * C::kTileBytes + x * 16384, &tq, &q_full[s], x * 64, hq, q0, b);
-        const size_t row0 = (size_t)(b * a.h + hq) * p.lq_pad + q0;
-        bulk_load(smem + C::kRowOff + s * 1024, p.lse2 + row0, kBM * 4, &q_full[s]);
-        bulk_load(smem + C::kRowOff + s * 1024 + 512, p.d_row + row0, kBM * 4, &q_full[s]);
-        if (it == 0) {
-          mbar_arrive_expect_tx(v_full, C::kTileBytes);
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(smem + C::kVOff + x * 16384, &tv, v_full, x * 64, kvh, sc.k0, b);
-        }
-        mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d(smem + C::kDOOff + s * C::kTileBytes + x * 16384, &tdo, &do_full[s], x * 64, hq, q0, b);
+        if (it >= 2 && !wait_parity(&qdo_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        issue_iter(it);
       }
       // loads still in flight must land before shared memory goes away
       volatile int no_abort = 0;

@@ -188,7 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (sc.hi_all < 0) sc.lo_all = sc.hi_all = 0;
 
   // ---- setup ----
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and sends the first loads (Q and the first K
+  // tiles, which wait on nothing) before the CTA-wide barrier, so that they are in flight while
+  // TMEM is allocated and the other warps arrive.
+  uint32_t qbytes = 0;        // producer lane: Q bytes in flight on q_full
+  int k_early = 0;            // producer lane: K tiles already issued
+  const uint64_t pol = l2_policy_evict_last();
+  if (threadIdx.x == kProducerWarp * 32) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
@@ -204,6 +210,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(mma_done, 1);
     for (int i = 0; i < kSub * C::kAccStages; ++i) mbar_init(&acc_full[i], 1);
     fence_mbar_init();
+    if (sc.hi_all > sc.lo_all) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+    }
+    if (kMerge) prefetch_tmap(&tacc);
+    if (kMerge ? p.fin.ptr != nullptr : !p.out_is_f32) prefetch_tmap(&tfin);
+    for (int t = 0; t < kSub; ++t)
+      if (sc.lo[t] < sc.hi[t]) qbytes += C::kTileBytes;
+    if (qbytes) {
+      mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < kSub; ++t) {
+        if (sc.lo[t] >= sc.hi[t]) continue;
+        uint8_t* dst = smem + C::kQOff + t * C::kTileBytes;
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(dst + x * 16384, &tq, q_full, x * 64, hq, sc.q0 + t * kBlockM, b);
+      }
+    }
+    for (; k_early < C::kStages && sc.lo_all + k_early < sc.hi_all; ++k_early) {
+      uint8_t* kd = smem + C::kKOff + k_early * C::kTileBytes;
+      mbar_arrive_expect_tx(&k_full[k_early], C::kTileBytes);
+      for (int x = 0; x < C::kBoxes; ++x)
+        tma_load_4d_hint(kd + x * 16384, &tk, &k_full[k_early], x * 64, kvh, (sc.lo_all + k_early) * kBlockN, b, pol);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
@@ -253,28 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ========================== TMA producer ==========================
     if (lane == 0) {
-      if (sc.hi_all > sc.lo_all) {
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
-      }
-      if (kMerge) prefetch_tmap(&tacc);
-      if (kMerge ? p.fin.ptr != nullptr : !p.out_is_f32) prefetch_tmap(&tfin);
-      uint32_t qbytes = 0;
-      for (int t = 0; t < kSub; ++t)
-        if (sc.lo[t] < sc.hi[t]) qbytes += C::kTileBytes;
-      if (qbytes) {
-        mbar_arrive_expect_tx(q_full, qbytes);
-        for (int t = 0; t < kSub; ++t) {
-          if (sc.lo[t] >= sc.hi[t]) continue;
-          uint8_t* dst = smem + C::kQOff + t * C::kTileBytes;
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(dst + x * 16384, &tq, q_full, x * 64, hq, sc.q0 + t * kBlockM, b);
-        }
-      }
-      const uint64_t pol = l2_policy_evict_last();
-      int it = 0;
-      for (int j = sc.lo_all; j < sc.hi_all; ++j, ++it) {
+      // (Q and the first K tiles went out during the setup)
+      int it = k_early;
+      for (int j = sc.lo_all + k_early; j < sc.hi_all; ++j, ++it) {
         const int s = it % C::kStages;
         if (it >= C::kStages) {
           if (!wait_parity(&k_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, p.status)) break;
