@@ -57,6 +57,7 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per iteration
 constexpr int kBN = 128;  // keys per CTA
+constexpr int kHeadBand = 4;  // K/V heads per band of the CTA order under a mask band
 constexpr int kThreads = 512;  // 4 warpgroups
 // Register split: launched at kRegsLaunch per thread (65536 / 512); the two
 // key-row warpgroups rise to kRegsCompute, the dQ drain and the producer/MMA
@@ -357,12 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = (a.lk + kBN - 1) / kBN;
   const bool full_band = a.wl >= a.lq - 1 && a.wr >= a.lk - 1;
   const bool head_major = full_band && a.h == a.hkv;
+  // Under a band the K/V heads of a batch go in bands of kHeadBand, one band after another, so
+  // that at most a band's Q/dO tiles and dQ rows are live in L2 at once; within a band the key
+  // blocks in ascending order with the band's K/V heads fastest.
   const int per_batch = nkb * a.hkv;
-  const int kb = head_major ? (int)(blockIdx.x % nkb) : (int)((blockIdx.x % per_batch) / a.hkv);
-  const int bkv = head_major ? (int)(blockIdx.x / nkb)
-                             : (int)(blockIdx.x / per_batch) * a.hkv + (int)(blockIdx.x % a.hkv);
-  const int b = bkv / a.hkv;
-  const int kvh = bkv % a.hkv;
+  int kb, kvh;
+  if (head_major) {
+    kb = (int)(blockIdx.x % nkb);
+    kvh = (int)((blockIdx.x / nkb) % a.hkv);
+  } else {
+    const int r = (int)(blockIdx.x % per_batch);
+    const int band = r / (kHeadBand * nkb);
+    const int h0 = band * kHeadBand;
+    const int bw = min(kHeadBand, a.hkv - h0);  // K/V heads in this band
+    const int rr = r - band * kHeadBand * nkb;
+    kb = rr / bw;
+    kvh = h0 + rr % bw;
+  }
+  const int b = (int)(blockIdx.x / per_batch);
   BwdSched sc;
   sc.k0 = kb * kBN;
   sc.g = a.h / a.hkv;
