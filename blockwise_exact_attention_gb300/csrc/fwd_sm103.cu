@@ -19,6 +19,12 @@
 //               per query row (TMEM lane), online softmax, P written back to
 //               TMEM over S as packed bf16, O rescaled in TMEM only when the
 //               row max grows by more than 2^8, and the final epilogue.
+//   warp 11     idle.
+// The epilogue stages O in shared memory and writes it out (TMA tensor stores
+// for a bf16 result). The fused ring step (kMerge) stages the caller's fp32
+// accumulator rows by TMA in the K/V stages as the last tiles free them,
+// folds the block into them in place by the log-sum-exp merge, and writes
+// them back by TMA.
 // The MMA issue order S_0(j), S_1(j), PV_0(j), S_0(j+1), PV_1(j), S_1(j+1),
 // ... lets each softmax group work while the tensor core serves the other
 // subtile. Tiles outside the causal/window band are never loaded or computed;
