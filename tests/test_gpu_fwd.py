@@ -140,3 +140,28 @@ def test_fwd_full_size_sampled(name):
     assert_close(to_np(lse.index_select(2, idx)), rl, TOL_LSE, "lse")
     # every row has at least its own key, so no output may be non-finite
     assert torch.isfinite(lse).all() and torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("d,causal,window,lk", [(128, False, (-1, -1), None), (64, False, (-1, -1), 3700),
+                                                (128, True, (300, 0), None), (64, False, (250, 60), None)])
+def test_fwd_many_blocks_ragged(d, causal, window, lk):
+    """320 CTAs (16 query blocks x 20 query heads over 4 K/V heads), more than two waves, with a
+    ragged last query block (4000 rows) and, for d=64, fewer keys than queries. Rows of every
+    query block and head against the oracle, and a second call gives the same bits."""
+    import blockwise_exact_attention_gb300 as bea
+    x = workloads.small_case(n=1, l=4000, h=20, h_kv=4, d=d, is_causal=causal, window=window, seed=140 + d,
+                             lk=lk)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (to_dev(x[s], torch.bfloat16) for s in ("q", "k", "v"))
+    out, lse = bea.flash_mha_fwd(q, k, v, scale, causal, window)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    rows = np.unique(np.concatenate([np.arange(0, 4000, 37), np.arange(3840, 4000, 11), [255, 256, 3999]]))
+    ro, rl = oracle.attention_fwd(x["q"], x["k"], x["v"], scale, causal, window, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    assert_close_bf16(to_np(out.index_select(1, idx)), ro, "out")
+    assert_close(to_np(lse.index_select(2, idx)), rl, TOL_LSE, "lse")
+    # and the same call again
+    out2, lse2 = bea.flash_mha_fwd(q, k, v, scale, causal, window)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
