@@ -226,3 +226,42 @@ def test_staged_bwd_accumulates_dq_over_kv_blocks(d):
     rdq, rdk, rdv = oracle.attention_bwd(x["dout"], x["q"], x["k"], x["v"], out_up, lse_up, scale, False)
     for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), (rdq, rdk, rdv)):
         assert_close_bf16(to_np(g), r, name, output_is_bf16=False)
+
+
+def test_beyond_int32_elements():
+    """q, out, dout and dq of 1,052,672 rows x 16 heads x 128 = 2.16e9 elements (past 2^31),
+    sliding window (64, 0), GQA 16/2, forward and backward (~27 GB on the device). The last 300
+    rows (the largest offsets) and 300 rows at 2^20 against the oracle on a sub-problem that
+    holds every key those rows see (key j at query position j - 64): out, lse and dQ of the
+    rows, dK/dV of the keys whose every query lies in the sub-problem."""
+    import blockwise_exact_attention_gb300 as bea
+    L, h, hkv, d, W = 1048576 + 4096, 16, 2, 128, 64
+    scale = 1.0 / math.sqrt(d)
+    gen = torch.Generator(device="cuda").manual_seed(4242)
+    q = torch.randn((1, L, h, d), generator=gen, device="cuda").to(torch.bfloat16)
+    k = torch.randn((1, L, hkv, d), generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn((1, L, hkv, d), generator=gen, device="cuda").to(torch.bfloat16)
+    do = torch.randn((1, L, h, d), generator=gen, device="cuda").to(torch.bfloat16)
+    assert q.numel() > 2 ** 31
+    out, lse = bea.flash_mha_fwd(q, k, v, scale, True, (W, 0))
+    dq, dk, dv = bea.flash_mha_bwd(do, q, k, v, out, lse, scale, True, (W, 0), grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert bea.device_status() == 0
+    assert torch.isfinite(lse).all() and torch.isfinite(out.float()).all()
+    for r0 in (L - 300, 1048576 - 150):
+        r1, k0 = r0 + 300, r0 - W
+        f32 = lambda t: t.float().cpu().numpy()
+        qs, ks, vs, dos = f32(q[:, r0:r1]), f32(k[:, k0:r1]), f32(v[:, k0:r1]), f32(do[:, r0:r1])
+        ro, rl = oracle.attention_fwd(qs, ks, vs, scale, True, (W, 0), key_offset=-W)
+        assert_close_bf16(to_np(out[:, r0:r1]), ro, "out")
+        assert_close(to_np(lse[:, :, r0:r1]), rl, TOL_LSE, "lse")
+        # the backward from the kernel's own out/lse of these rows
+        rdq, rdk, rdv = oracle.attention_bwd(dos, qs, ks, vs, f32(out[:, r0:r1]), f32(lse[:, :, r0:r1]), scale, True,
+                                             (W, 0), key_offset=-W)
+        assert_close_bf16(to_np(dq[:, r0:r1]), rdq, "dq", output_is_bf16=False)
+        # a key is read by the queries up to W after it: complete where those all lie in the rows
+        ke = r1 if r1 == L else r1 - W
+        assert_close_bf16(to_np(dk[:, r0:ke]), rdk[:, W:W + ke - r0], "dk", output_is_bf16=False)
+        assert_close_bf16(to_np(dv[:, r0:ke]), rdv[:, W:W + ke - r0], "dv", output_is_bf16=False)
+    del q, k, v, do, out, lse, dq, dk, dv
+    torch.cuda.empty_cache()
