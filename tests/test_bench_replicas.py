@@ -1,6 +1,6 @@
-"""The replica bookkeeping of bench.py on CPU: two gloo ranks, the slowest
-rank's time sets the whole-job figure, and the reference arm prints only on
-rank 0."""
+"""bench.py on CPU: the replica bookkeeping (two gloo ranks, the slowest
+rank's time sets the whole-job figure), the reference arm's JSON line (printed only on
+rank 0), and a kernel arm that fails loudly without a GPU."""
 
 import os
 import socket
@@ -56,3 +56,35 @@ def test_reference_arm_prints_only_on_rank_0(repo_root):
     r = subprocess.run([sys.executable, os.path.join(repo_root, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "0", "--gpus", "2"], capture_output=True, text=True, env=env, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_json_line(repo_root):
+    """The reference arm (the fp64 oracle on a bounded sample, host cores) prints one JSON line
+    with the contract's keys; its value, cpu_baseline and e2e agree and it copies nothing."""
+    import json
+    r = subprocess.run([sys.executable, os.path.join(repo_root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
+    assert d["higher_is_better"] is True and d["unit"] == "TFLOP/s" and d["dtype"] == "f64"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert "workload" in d["config"]
+
+
+def test_gpu_arm_fails_loudly_without_a_gpu(repo_root):
+    """With no GPU the kernel arm exits non-zero; nothing stands in for the CUDA path."""
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    r = subprocess.run([sys.executable, os.path.join(repo_root, "bench.py"), "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert not any(ln.startswith("{") for ln in r.stdout.splitlines())
