@@ -198,52 +198,59 @@ __global__ void __launch_bounds__(kRowThreads) bwd_preprocess_kernel(BwdParams p
 
 // dq = scale * accumulator, cast to bf16, written, or added to an fp32 dq. The
 // accumulator is [n h][lq_pad / 4][D][4] (four query rows interleaved per
-// head-dim index); a thread takes 8 head-dim entries of a group of four rows:
-// 128 contiguous bytes in, four 8-entry row pieces out.
+// head-dim index). A thread takes two consecutive head-dim entries of a group of
+// four rows, 32 contiguous bytes: a warp reads one contiguous 1 KB span and
+// writes 64 consecutive entries of each of the four rows. Every thread keeps two
+// groups in flight.
 template <int D>
 __global__ void __launch_bounds__(kRowThreads) bwd_convert_dq_kernel(BwdParams p) {
-  constexpr int kTpg = D / 8;
-  constexpr int kGroupsPerPass = kRowThreads / kTpg;
+  constexpr int kTpg = D / 2;                         // threads per group of four rows
+  constexpr int kGroupsPerPass = kRowThreads / kTpg;  // groups of a block's pass, per half
   const AttnDims& a = p.a;
   const int64_t groups_bh = (a.lq + 3) / 4;
   const int64_t total = (int64_t)a.n * a.h * groups_bh;
   const int sub = threadIdx.x / kTpg;
-  const int c = (threadIdx.x % kTpg) * 8;
-  const int64_t stride = (int64_t)gridDim.x * kGroupsPerPass;
-  for (int64_t g0 = (int64_t)blockIdx.x * kGroupsPerPass + sub; g0 < total; g0 += stride) {
-    const int64_t bh = g0 / groups_bh;
-    const int gi = (int)(g0 % groups_bh);
-    const float* acc = p.dq_acc + (((size_t)bh * (p.lq_pad / 4) + gi) * D + c) * 4;
-    float4 q4[8];  // q4[k]: the four rows at head-dim entry c + k
+  const int e = (threadIdx.x % kTpg) * 2;  // head-dim entries e and e + 1
+  const int64_t stride = (int64_t)gridDim.x * kGroupsPerPass * 2;
+  for (int64_t g0 = (int64_t)blockIdx.x * kGroupsPerPass * 2 + sub; g0 < total; g0 += stride) {
+    const int64_t gs[2] = {g0, g0 + kGroupsPerPass};
+    float4 q4[2][2];  // [u][k]: the four rows of group gs[u] at entry e + k
 #pragma unroll
-    for (int k = 0; k < 8; ++k) q4[k] = *reinterpret_cast<const float4*>(acc + 4 * k);
-    const int hq = (int)(bh % a.h), b = (int)(bh / a.h);
+    for (int u = 0; u < 2; ++u) {
+      if (gs[u] >= total) continue;
+      const int64_t bh = gs[u] / groups_bh;
+      const int64_t gi = gs[u] % groups_bh;
+      const float* acc = p.dq_acc + ((size_t)bh * (p.lq_pad / 4) + gi) * (D * 4) + e * 4;
+      q4[u][0] = *reinterpret_cast<const float4*>(acc);
+      q4[u][1] = *reinterpret_cast<const float4*>(acc + 4);
+    }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = 4 * gi + r;
-      if (i >= a.lq) break;
-      float v[8];
+    for (int u = 0; u < 2; ++u) {
+      if (gs[u] >= total) continue;
+      const int64_t bh = gs[u] / groups_bh;
+      const int gi = (int)(gs[u] % groups_bh);
+      const int hq = (int)(bh % a.h), b = (int)(bh / a.h);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = (r == 0 ? q4[k].x : r == 1 ? q4[k].y : r == 2 ? q4[k].z : q4[k].w) * a.scale;
-      if (p.dq_is_f32) {
-        float* dst = reinterpret_cast<float*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
-        if (p.accumulate) {
-          const float4 lo = *reinterpret_cast<const float4*>(dst);
-          const float4 hi = *reinterpret_cast<const float4*>(dst + 4);
-          v[0] += lo.x; v[1] += lo.y; v[2] += lo.z; v[3] += lo.w;
-          v[4] += hi.x; v[5] += hi.y; v[6] += hi.z; v[7] += hi.w;
+      for (int r = 0; r < 4; ++r) {
+        const int i = 4 * gi + r;
+        if (i >= a.lq) break;
+        const float4& x0 = q4[u][0];
+        const float4& x1 = q4[u][1];
+        float v0 = (r == 0 ? x0.x : r == 1 ? x0.y : r == 2 ? x0.z : x0.w) * a.scale;
+        float v1 = (r == 0 ? x1.x : r == 1 ? x1.y : r == 2 ? x1.z : x1.w) * a.scale;
+        if (p.dq_is_f32) {
+          float* dst = reinterpret_cast<float*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + e;
+          if (p.accumulate) {
+            const float2 old = *reinterpret_cast<const float2*>(dst);
+            v0 += old.x;
+            v1 += old.y;
+          }
+          *reinterpret_cast<float2*>(dst) = make_float2(v0, v1);
+        } else {
+          __nv_bfloat16* dst =
+              reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + e;
+          *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(v0, v1);
         }
-        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
-      } else {
-        __nv_bfloat16* dst =
-            reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sn + (int64_t)i * p.dq.sl + hq * p.dq.sh + c;
-        uint4 raw;
-        raw.x = pack_bf16x2(v[0], v[1]);
-        raw.y = pack_bf16x2(v[2], v[3]);
-        raw.z = pack_bf16x2(v[4], v[5]);
-        raw.w = pack_bf16x2(v[6], v[7]);
-        *reinterpret_cast<uint4*>(dst) = raw;
       }
     }
   }
@@ -928,8 +935,9 @@ cudaError_t launch_bwd_finish(const BwdParams& p, cudaStream_t s, int* nlaunch) 
   const bool d128 = p.a.d == 128;
   auto kern = d128 ? bwd_convert_dq_kernel<128> : bwd_convert_dq_kernel<64>;
   unsigned grid = 0;
-  // row_grid counts two rows per thread group and pass; the convert takes one group of four
-  cudaError_t e = row_grid(d128 ? cap128 : cap64, kern, 2 * groups, p.a.d, &grid);
+  // row_grid sizes a block for 2 x 256 / (d / 8) rows; a block of the convert takes 2 x 512 / d
+  // groups of four rows per pass, a quarter as many
+  cudaError_t e = row_grid(d128 ? cap128 : cap64, kern, 4 * groups, p.a.d, &grid);
   if (e != cudaSuccess) return e;
   kern<<<grid, kRowThreads, 0, s>>>(p);
   *nlaunch += 1;

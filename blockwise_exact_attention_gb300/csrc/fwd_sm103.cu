@@ -414,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             BEA_ISSUE_PV(0, s, pv0 == 0);
             ++pv0;
+            // O_0 is final once its last P V completes: subtile 0's epilogue need not wait for
+            // subtile 1's last softmax and P V
+            if (j == hi0 - 1) umma_commit_warp(&o_full[0]);
           }
           if (n0) {
             if (!(ok = warp_wait_parity(&k_full[s1], par1, abort_flag, p.status))) break;
@@ -436,7 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j + 1 < hi_all) umma_commit_warp(&k_empty[s1]);  // every S of tile j+1 is issued
           umma_commit_warp(&v_empty[s]);                       // every P V of tile j is issued
-          if (j == hi0 - 1) umma_commit_warp(&o_full[0]);
           if (j == hi1 - 1) umma_commit_warp(&o_full[1]);
         }
       }
