@@ -91,6 +91,12 @@ def test_bwd_bf16_gradients():
     run_bwd(x, 1.0 / math.sqrt(128), True, (-1, -1), torch.bfloat16)
 
 
+def test_bwd_bf16_gradients_d64_ragged():
+    """bf16 dq/dk/dv at d = 64 with lq = 4k + 3 (the dQ conversion's last group of four rows is partial)."""
+    x = workloads.small_case(n=2, l=259, h=4, h_kv=2, d=64, is_causal=False, window=(50, 10), seed=23)
+    run_bwd(x, 1.0 / math.sqrt(64), False, (50, 10), torch.bfloat16)
+
+
 def test_bwd_accumulate():
     x = workloads.small_case(n=1, l=257, h=2, h_kv=2, d=64, seed=22)
     run_bwd(x, 0.125, True, (-1, -1), torch.float32, accumulate=True)
