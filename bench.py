@@ -518,13 +518,21 @@ def main():
     qr = torch.randn((1, wr.l, wr.h, wr.d), device=dev).to(torch.bfloat16)
     kr = torch.randn_like(qr)
     vr = torch.randn_like(qr)
-    ring_ms = statistics.median(timed(lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True),
-                                      5, 2))
-    # the unfused replay: each block written out in bf16, then ring_merge
-    ring_unfused_ms = statistics.median(timed(lambda: bea.ring_attention_fwd(
-        qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True, block_dtype=torch.bfloat16, fused=False), 5, 2))
+    # the ring replay, its unfused form (each block written out in bf16, then ring_merge) and the
+    # single call on the same problem, timed in turn within each repetition so that all three
+    # see the same clocks
+    ring_fns = (lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True),
+                lambda: bea.ring_attention_fwd(qr, kr, vr, wr.ring_chunks, wr.softmax_scale, True,
+                                               block_dtype=torch.bfloat16, fused=False),
+                lambda: bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True))
+    for fn in ring_fns:
+        timed(fn, 0, 2)
+    ring_ts = [[], [], []]
+    for _ in range(9):
+        for i, fn in enumerate(ring_fns):
+            ring_ts[i] += timed(fn, 1, 0)
+    ring_ms, ring_unfused_ms, single_ms = (statistics.median(t) for t in ring_ts)
     rf, rb = attention_flops(1, wr.h, wr.l, wr.l, wr.d, True)
-    single_ms = statistics.median(timed(lambda: bea.flash_mha_fwd(qr, kr, vr, wr.softmax_scale, True), 5, 2))
 
     # host time to issue one ring replay (the calls return before the GPU is done): the library
     # call issuing all 8 steps, against the same replay composed from Python (forward + merge calls)
@@ -545,12 +553,18 @@ def main():
     bea.launches_since_reset(reset=True)
     bea.ring_attention_bwd(dor, qr, kr, vr, o_r, l_r, wr.ring_chunks, wr.softmax_scale, True)
     ring_bwd_launches = bea.launches_since_reset(reset=True)
-    ring_bwd_ms = statistics.median(timed(lambda: bea.ring_attention_bwd(dor, qr, kr, vr, o_r, l_r, wr.ring_chunks,
-                                                                         wr.softmax_scale, True), 5, 2))
     wsr = torch.empty(bea.bwd_workspace_bytes(qr), dtype=torch.uint8, device=dev)
     gr = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (qr, kr, vr)]
-    single_bwd_ms = statistics.median(timed(lambda: bea.flash_mha_bwd(
-        dor, qr, kr, vr, o_r, l_r, wr.softmax_scale, True, dq=gr[0], dk=gr[1], dv=gr[2], workspace=wsr), 5, 2))
+    bwd_fns = (lambda: bea.ring_attention_bwd(dor, qr, kr, vr, o_r, l_r, wr.ring_chunks, wr.softmax_scale, True),
+               lambda: bea.flash_mha_bwd(dor, qr, kr, vr, o_r, l_r, wr.softmax_scale, True, dq=gr[0], dk=gr[1],
+                                         dv=gr[2], workspace=wsr))
+    for fn in bwd_fns:
+        timed(fn, 0, 2)
+    bwd_ts = [[], []]
+    for _ in range(5):  # in turn, as for the forward
+        for i, fn in enumerate(bwd_fns):
+            bwd_ts[i] += timed(fn, 1, 0)
+    ring_bwd_ms, single_bwd_ms = (statistics.median(t) for t in bwd_ts)
     del qr, kr, vr, acc, lacc, blk, lblk, dor, o_r, l_r, wsr, gr
 
     # ---- the other workloads of the measurement plan: forward and backward alone ----
