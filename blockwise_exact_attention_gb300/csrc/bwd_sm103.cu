@@ -426,7 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The producer's lane initialises the barriers and sends the loads that wait on nothing (K and
   // the first two iterations' Q/dO) before the CTA-wide barrier, so that they are in flight while
   // TMEM is allocated and the other warps arrive.
+  // The barriers of the first loads (K, V, Q/dO of two stages: bars[0, 6)) are the producer
+  // lane's; the warp's other lanes initialise the rest meanwhile, one each.
   int it_early = 0;  // producer lane: iterations already issued
+  constexpr int kFirstBars = 6;
+  if (warp == kProducerWarp && lane > 0 && lane <= C::kNumBars - kFirstBars) {
+    uint64_t* bar = &bars[kFirstBars + lane - 1];
+    mbar_init(bar, (bar == &dq_empty[0] || bar == &dq_empty[1]) ? 128 : 1);
+    fence_mbar_init();
+  }
   if (threadIdx.x == kProducerWarp * 32) {
     *abort_flag = 0;
     mbar_init(k_full, 1);
@@ -434,13 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&do_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
-      mbar_init(&sp_full[s], 1);
-      mbar_init(&dq_full[s], 1);
-      mbar_init(&dq_empty[s], 128);
     }
-    mbar_init(dkv_full, 1);
-    mbar_init(mma_done, 1);
     fence_mbar_init();
     if (sc.n_iter > 0) {
       prefetch_tmap(&tq);

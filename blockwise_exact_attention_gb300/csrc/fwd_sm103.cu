@@ -194,27 +194,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (sc.hi_all < 0) sc.lo_all = sc.hi_all = 0;
 
   // ---- setup ----
-  // The producer's lane initialises the barriers and sends the first loads (Q and the first K
-  // tiles, which wait on nothing) before the CTA-wide barrier, so that they are in flight while
-  // TMEM is allocated and the other warps arrive.
+  // The producer's lane initialises the barriers of the first loads (q_full, k_full) and sends
+  // those loads (Q and the first K tiles, which wait on nothing) before the CTA-wide barrier, so
+  // that they are in flight while TMEM is allocated and the other warps arrive; meanwhile the
+  // warp's other lanes initialise the remaining barriers, one each (every barrier counts one
+  // arrival).
   uint32_t qbytes = 0;        // producer lane: Q bytes in flight on q_full
   int k_early = 0;            // producer lane: K tiles already issued
   const uint64_t pol = l2_policy_evict_last();
+  constexpr int kFirstBars = 1 + C::kStages;  // q_full, k_full[0, kStages): bars[0, kFirstBars)
+  static_assert(C::kNumBars - kFirstBars <= 31, "one remaining barrier per lane");
+  if (warp == kProducerWarp && lane > 0 && lane <= C::kNumBars - kFirstBars) {
+    mbar_init(&bars[kFirstBars + lane - 1], 1);
+    fence_mbar_init();
+  }
   if (threadIdx.x == kProducerWarp * 32) {
     *abort_flag = 0;
-    mbar_init(q_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int t = 0; t < kSub; ++t) {
-      mbar_init(&s_full[t], 1);
-      mbar_init(&o_full[t], 1);
-    }
-    mbar_init(mma_done, 1);
-    for (int i = 0; i < kSub * C::kAccStages; ++i) mbar_init(&acc_full[i], 1);
+    for (int i = 0; i < kFirstBars; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     if (sc.hi_all > sc.lo_all) {
       prefetch_tmap(&tq);
