@@ -43,11 +43,11 @@ L2_FLUSH_BYTES = 256 << 20
 # figure no longer describes the kernel, and the JSON line reports null.
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, source hash at capture)
-    "bwd_bf16_kernel<128>": (355.4e6 + 144.1e6, "c150b0ce0c64"),   # causal GQA 8k, one launch
-    "fwd_bf16_kernel<128>": (101.1e6 + 36.3e6, "84da8d91095d"),    # causal GQA 8k, one launch
+    "bwd_bf16_kernel<128>": (354.9e6 + 144.5e6, "1f52ed6e8886"),   # causal GQA 8k, one launch
+    "fwd_bf16_kernel<128>": (101.0e6 + 36.4e6, "eda1cfd6e9a0"),    # causal GQA 8k, one launch
     "ring_merge_kernel": (204.1e6 + 76.2e6, "531d70872b16"),       # [1,16384,16,128], L2 flushed before
     # the fused ring step of the 16k ring, step 1 (7 chunk pairs, 896 CTAs); same sources as the forward
-    "fwd_bf16_kernel<128, merge>": (294.8e6 + 90.2e6, "84da8d91095d"),
+    "fwd_bf16_kernel<128, merge>": (294.7e6 + 90.3e6, "eda1cfd6e9a0"),
 }
 # Algorithmic bytes of that fused step: q, k, v (bf16) of 7 chunks of [2048, 16, 128], the fp32
 # accumulator read and written, the log-sum-exp read and written.
