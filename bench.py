@@ -285,6 +285,18 @@ def run_only(which, fwd, bwd, dev, workloads, bea):
         oo, lo_ = bea.flash_mha_fwd(qo, ko, vo, wo.softmax_scale, wo.is_causal, wo.window)
         for _ in range(4):
             bea.flash_mha_bwd(doo, qo, ko, vo, oo, lo_, wo.softmax_scale, wo.is_causal, wo.window)
+    elif which in ("swa_fwd", "swa_bwd"):
+        # the sliding-window workload (1024, 0) [1,32768,32,128] of the measurement plan
+        wo = workloads.WORKLOADS["swa_32k_d128"]
+        qo = torch.randn((wo.n, wo.l, wo.h, wo.d), device=dev).to(torch.bfloat16)
+        ko = torch.randn((wo.n, wo.l, wo.h_kv, wo.d), device=dev).to(torch.bfloat16)
+        vo, doo = torch.randn_like(ko), torch.randn_like(qo)
+        oo, lo_ = bea.flash_mha_fwd(qo, ko, vo, wo.softmax_scale, wo.is_causal, wo.window)
+        for _ in range(4):
+            if which == "swa_fwd":
+                bea.flash_mha_fwd(qo, ko, vo, wo.softmax_scale, wo.is_causal, wo.window)
+            else:
+                bea.flash_mha_bwd(doo, qo, ko, vo, oo, lo_, wo.softmax_scale, wo.is_causal, wo.window)
     elif which in ("ring", "ring_unfused", "ring_bwd"):
         # the 16k causal ring replay (8 chunks): two forward replays, or two backward replays
         wr = workloads.WORKLOADS["ring_causal_16k"]
@@ -320,10 +332,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fwd", "bwd", "merge", "bwd_d64", "ring", "ring_unfused", "ring_bwd"],
+    ap.add_argument("--only", choices=["fwd", "bwd", "merge", "bwd_d64", "swa_fwd", "swa_bwd", "ring", "ring_unfused",
+                                       "ring_bwd"],
                     help="run just this kernel a few times on the bench workload, bwd_d64 on the d=64 "
-                         "full-attention workload, or two ring replays of the 16k causal workload "
-                         "(for profiler captures)")
+                         "full-attention workload, swa_* on the sliding-window workload, or two ring replays "
+                         "of the 16k causal workload (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
